@@ -1,0 +1,81 @@
+"""FLOP and byte accounting for the MoE expert-layer forward.
+
+Used by the benchmark to turn measured times into roofline fractions.
+
+* FLOPs are algorithmic: only routed tokens count, 2*T*k*3*H*F for the three
+  expert GEMMs (FC1 gate and up: H->F each; FC2: F->H).  The expert FFN is the
+  SwiGLU expert with three d x dffn matrices ("Piper", §III-A, Table III).
+* Bytes are what the layer must move at least once: the weights of every
+  expert that receives a token, plus x, the output and the router logits.
+* util = min(topk/E * B/F * b, 1) is the utilisation model of the expert
+  GEMMs for a batch of b tokens ("MegaScale-Infer", §2 Context and
+  Motivation).  Its ridge b* = F/B is the batch at which a GEMM stops being
+  bandwidth-bound.
+"""
+from __future__ import annotations
+
+BF16 = 2
+FP32 = 4
+INT32 = 4
+
+
+def ffn_flops(T: int, H: int, F: int, k: int) -> int:
+    """Algorithmic FLOPs of the expert FFNs: 2 * T*k * 3*H*F."""
+    return 2 * T * k * 3 * H * F
+
+
+def expert_weight_bytes(H: int, F: int, n_experts: int, elem: int = BF16) -> int:
+    """Bytes of n_experts SwiGLU experts (three H x F matrices each)."""
+    return 3 * H * F * elem * n_experts
+
+
+def layer_bytes(T: int, H: int, F: int, E: int, k: int, touched_experts: int) -> int:
+    """Minimum HBM bytes of one layer forward: touched weights + x (bf16) +
+    out (bf16) + logits (fp32)."""
+    return (expert_weight_bytes(H, F, touched_experts) + T * H * BF16 + T * H * BF16
+            + T * E * FP32)
+
+
+def roofline_seconds(flops: float, nbytes: float, peak_flops: float, peak_bw: float):
+    """(t_roof, bound) with t_roof = max(flops/peak_flops, bytes/peak_bw)."""
+    tc, tm = flops / peak_flops, nbytes / peak_bw
+    return (tc, "tensor") if tc >= tm else (tm, "hbm")
+
+
+def ridge_tokens(peak_flops: float, peak_bw: float) -> float:
+    """Batch size b* at which util reaches 1 for a dense GEMM: F/B."""
+    return peak_flops / peak_bw
+
+
+def util(topk: int, n_expert: int, peak_bw: float, peak_flops: float, b: float) -> float:
+    """min(topk/#expert * B/F * b, 1)."""
+    return min(topk / n_expert * peak_bw / peak_flops * b, 1.0)
+
+
+# Per-kernel algorithmic bytes (one launch) ---------------------------------
+def route_bytes(T: int, E: int, k: int) -> int:
+    """logits read + topk_idx and topk_w written."""
+    return T * E * FP32 + T * k * (INT32 + FP32)
+
+
+def permute_bytes(T: int, k: int, H: int) -> int:
+    """topk_idx read twice (count, scatter) + sorted_src, dest_of written +
+    the x rows gathered into expert order (read and written)."""
+    P = T * k
+    return 2 * P * INT32 + 2 * P * INT32 + 2 * P * H * BF16
+
+
+def fc1_bytes(H: int, F: int, touched: int, P: int) -> int:
+    """W1 and W3 of touched experts + gathered x rows read + h written."""
+    return 2 * H * F * BF16 * touched + P * H * BF16 + P * F * BF16
+
+
+def fc2_bytes(H: int, F: int, touched: int, P: int) -> int:
+    """W2 of touched experts + h read + y_sorted written."""
+    return H * F * BF16 * touched + P * F * BF16 + P * H * BF16
+
+
+def combine_bytes(T: int, H: int, k: int) -> int:
+    """y_sorted rows read + out written + dest_of and topk_w read."""
+    P = T * k
+    return P * H * BF16 + T * H * BF16 + P * (INT32 + FP32)
