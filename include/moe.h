@@ -1,0 +1,189 @@
+/*
+ * libmoe -- C ABI of the MoE expert-layer forward on one GPU (sm_103a).
+ *
+ * The layer:  out[t] = sum_{j<k} w[t,j] * FFN_{e[t,j]}(x[t]),
+ *             FFN_e(x) = (silu(x W1[e]) * (x W3[e])) W2[e],
+ * computed as four steps -- top-k gating, scatter into per-expert groups,
+ * per-expert SwiGLU FFN, weighted return to token order -- following
+ * "MegaScale-Infer: Serving Mixture-of-Experts at Scale with Disaggregated
+ * Expert Parallelism" (§3.2 Big-Picture Architecture, steps (1)-(5);
+ * §3.4 Supporting Implementation Details, Fused Kernels, steps (1)-(4)),
+ * "MegaFlux: Skew-Resilient MoE Megakernels via Pipelined Expert
+ * Replication" (§2.1, §3.1, §A.2) and "Piper: Efficient Large-Scale MoE
+ * Training via Resource Modeling and Pipelined Hybrid Parallelism"
+ * (§III-A, Table III).
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *     contiguous, 16-byte aligned.  bf16 tensors are passed as void* and
+ *     hold IEEE bfloat16 (__nv_bfloat16) values.  The library never
+ *     allocates, frees or keeps a reference to caller memory beyond a call.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on `stream` and returns; nothing synchronises
+ *     except moe_get_device_status.
+ *   - `ws` is a caller-owned device workspace of at least
+ *     moe_workspace_size(T, H, F, E, k) bytes, 256-byte aligned.  It holds
+ *     the intermediates and a device status word.  Calls that share one
+ *     workspace must not overlap in time (use one stream per workspace).
+ *   - Limits: 0 <= T, T*k < 2^31; 1 <= E <= MOE_MAX_EXPERTS;
+ *     1 <= k <= min(E, MOE_MAX_TOPK); H and F positive multiples of 128.
+ *     Violations are reported synchronously as MOE_ERR_INVALID_ARG and
+ *     nothing is enqueued.  T == 0 is a valid no-op.
+ *   - Conditions only the device can see (a non-finite router logit, a
+ *     pipeline wait that ran out) are written to the status word in `ws`
+ *     and read back with moe_get_device_status; the kernels never trap.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad size, null or misaligned pointer       */
+  MOE_ERR_NONFINITE = 2,    /* a router logit is NaN or +-inf (device)    */
+  MOE_ERR_TIMEOUT = 3,      /* a bounded device wait ran out (device)     */
+  MOE_ERR_WORKSPACE = 4,    /* ws is NULL, too small or misaligned        */
+  MOE_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed       */
+  MOE_ERR_UNSUPPORTED = 6   /* no sm_103a device is current               */
+} moe_status;
+
+/* Bytes of workspace needed for a layer of these sizes (0 on bad sizes). */
+size_t moe_workspace_size(int T, int H, int F, int E, int k);
+
+/*
+ * Step 1 -- top-k gating and weight normalisation
+ * ("MegaScale-Infer", §3.4 Fused Kernels, steps (1) and (3)).
+ *
+ *   logits   [T, E] fp32 router output.
+ *   topk_idx [T, k] int32 out: slot j is the j-th largest logit of the token;
+ *            equal logits (also -0.0 vs +0.0) go to the lower expert index.
+ *   topk_w   [T, k] fp32 out: softmax over the k selected logits (they sum
+ *            to 1).
+ * A NaN or infinite logit sets MOE_ERR_NONFINITE in the device status; the
+ * outputs of that token are then unspecified.
+ */
+moe_status moe_route_topk(const float* logits, int T, int E, int k,
+                          int32_t* topk_idx, float* topk_w,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Step 2 -- per-expert counts and the stable scatter into expert groups
+ * ("MegaScale-Infer", §3.4 Fused Kernels, steps (2) and (4); order inside an
+ * expert by token, then top-k position: "MegaFlux", §A.2).
+ *
+ * Assignment a = t*k + j.
+ *   topk_idx   [T, k] int32 in, values in [0, E).
+ *   counts     [E]    int32 out: assignments per expert (sum = T*k).
+ *   offsets    [E+1]  int32 out: exclusive prefix sum of counts.
+ *   sorted_src [T*k]  int32 out: sorted_src[p] = a, p ascending within each
+ *              expert's range [offsets[e], offsets[e+1]) in ascending a.
+ *   dest_of    [T*k]  int32 out: inverse map, sorted_src[dest_of[a]] == a.
+ * Deterministic: bit-identical on every run.  An out-of-range expert index
+ * gives MOE_ERR_INVALID_ARG in the device status and unspecified outputs.
+ */
+moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k,
+                       int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_src, int32_t* dest_of,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Step 3 -- per-expert SwiGLU FFN as a grouped GEMM over the expert groups
+ * ("Piper", §III-A: W_gate, W_up in R^{d x dffn}, W_down in R^{dffn x d};
+ * "MegaScale-Infer", §3.4 Performance Simulation Model: FFN Input and FFN
+ * Output GEMMs; tile-aligned token blocks of at most 128 rows per expert,
+ * at most one partial block per expert: "MegaFlux", §3.1).
+ *
+ *   x          [T, H] bf16.
+ *   sorted_src [T*k], offsets [E+1] as produced by moe_permute.
+ *   W1, W3     [E, H, F] bf16: gate (silu applied) and up projections.
+ *   W2         [E, F, H] bf16: down projection.
+ *   y_sorted   [T*k, H] bf16 out: y_sorted[p] = FFN_e(x[sorted_src[p]/k])
+ *              for p in expert e's range.
+ * bf16 operands, fp32 accumulation, SwiGLU applied to the fp32 accumulators;
+ * the intermediate h = silu(g)*u is stored in bf16.
+ */
+moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src,
+                           const int32_t* offsets,
+                           const void* W1, const void* W3, const void* W2,
+                           int T, int H, int F, int E, int k,
+                           void* y_sorted, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Step 4 -- weighted return to token order
+ * ("MegaFlux", §2.1 final top-k sum; "MegaScale-Infer", §3.2 step (4)).
+ *
+ *   out[t] = sum_{j<k} topk_w[t,j] * y_sorted[dest_of[t*k+j]], summed in
+ *   slot order in fp32 and rounded once to bf16.
+ *   y_sorted [T*k, H] bf16, dest_of [T*k] int32, topk_w [T, k] fp32,
+ *   out [T, H] bf16 out.  No workspace.
+ */
+moe_status moe_combine(const void* y_sorted, const int32_t* dest_of,
+                       const float* topk_w, int T, int H, int k,
+                       void* out, void* stream);
+
+/*
+ * The whole layer: steps 1-4 on `stream`, intermediates in `ws`.
+ *   x [T, H] bf16, router_logits [T, E] fp32, W1/W3 [E, H, F] bf16,
+ *   W2 [E, F, H] bf16, out [T, H] bf16.
+ * The device status word is cleared at the start of the call.
+ */
+moe_status moe_forward(const void* x, const float* router_logits,
+                       const void* W1, const void* W3, const void* W2,
+                       int T, int H, int F, int E, int k, void* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer with the per-step activations in HOST memory: copies
+ * x_host [T, H] bf16 and logits_host [T, E] fp32 to the device, runs
+ * moe_forward, and copies the result back to out_host [T, H] bf16.  The
+ * weights are device pointers (resident model parameters).  Host buffers
+ * should be page-locked for the copies to be asynchronous; out_host is
+ * valid once `stream` has been synchronised.  The staging buffers live in
+ * `ws` (moe_workspace_size covers them).
+ */
+moe_status moe_forward_host(const void* x_host, const float* logits_host,
+                            const void* W1, const void* W3, const void* W2,
+                            int T, int H, int F, int E, int k, void* out_host,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward with timing marks: records events[0] on `stream` before the
+ * first kernel and events[i] after stage i, for the MOE_FORWARD_STAGES
+ * stages route, scan, scatter, gather, fc1, fc2, combine (in that order).
+ * `events` points to MOE_FORWARD_STAGES + 1 cudaEvent_t created by the
+ * caller.  Same arguments, work and results as moe_forward.
+ */
+#define MOE_FORWARD_STAGES 7
+moe_status moe_forward_events(const void* x, const float* router_logits,
+                              const void* W1, const void* W3, const void* W2,
+                              int T, int H, int F, int E, int k, void* out,
+                              void* ws, size_t ws_bytes, void* const* events,
+                              void* stream);
+
+/* Name of timing stage i of moe_forward_events (NULL if out of range). */
+const char* moe_forward_stage_name(int i);
+
+/*
+ * Synchronises `stream` and returns the device status word of `ws`
+ * (MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_INVALID_ARG), or
+ * MOE_ERR_CUDA if the synchronisation itself failed.
+ */
+moe_status moe_get_device_status(const void* ws, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

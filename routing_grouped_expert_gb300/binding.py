@@ -1,0 +1,265 @@
+"""ctypes binding of libmoe.so: the same entry points as include/moe.h, taking
+torch tensors.  This layer only checks shapes, dtypes and devices and passes
+raw pointers, sizes and the current CUDA stream; all computation runs in the
+library's kernels.  A missing or unloadable library raises MoeError: there is
+no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_NONFINITE",
+                3: "MOE_ERR_TIMEOUT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
+                6: "MOE_ERR_UNSUPPORTED"}
+
+# Every symbol include/moe.h declares, with its ctypes signature.
+_VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_route_topk": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_permute": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_grouped_ffn": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ,
+                             _VP]),
+    "moe_combine": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP, _VP]),
+    "moe_forward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_forward_host": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ,
+                              _VP]),
+    "moe_forward_events": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ,
+                                _VP, _VP]),
+    "moe_forward_stage_name": (ctypes.c_char_p, [_I]),
+    "moe_get_device_status": (_I, [_VP, _VP]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        name = STATUS_NAMES.get(code, str(code))
+        super().__init__(f"{what}: {name}")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libmoe.so once and declare its signatures."""
+    global _lib
+    if _lib is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise MoeError(-1, f"libmoe.so is not built ({p}); run "
+                               "`python -m routing_grouped_expert_gb300.build`")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != MOE_OK:
+        raise MoeError(code, what)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, shape, name: str, cuda: bool = True):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+class Workspace:
+    """A reusable device workspace (grows on demand, 256-byte aligned)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self.buf = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
+_default_ws: dict = {}
+
+
+def _ws(ws: Workspace | None, nbytes: int) -> Workspace:
+    if ws is None:
+        dev = torch.cuda.current_device()
+        ws = _default_ws.setdefault(dev, Workspace(torch.device("cuda", dev)))
+    ws.ensure(nbytes)
+    return ws
+
+
+# ------------------------------------------------------------ entry points
+def moe_workspace_size(T: int, H: int, F: int, E: int, k: int) -> int:
+    return int(load_library().moe_workspace_size(T, H, F, E, k))
+
+
+def moe_status_string(code: int) -> str:
+    return load_library().moe_status_string(code).decode()
+
+
+def moe_get_device_status(ws: Workspace) -> int:
+    """Synchronises the current stream; returns the device status word."""
+    return int(load_library().moe_get_device_status(ws.ptr, _stream()))
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None,
+                   ws: Workspace | None = None):
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    topk_idx = torch.empty(T, k, dtype=torch.int32, device=logits.device) \
+        if topk_idx is None else topk_idx
+    topk_w = torch.empty(T, k, dtype=torch.float32, device=logits.device) \
+        if topk_w is None else topk_w
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    ws = _ws(ws, 256)
+    _check(load_library().moe_route_topk(_p(logits), T, E, k, _p(topk_idx), _p(topk_w), ws.ptr,
+                                         ws.nbytes, _stream()), "moe_route_topk")
+    return topk_idx, topk_w
+
+
+def moe_permute(topk_idx: torch.Tensor, E: int, ws: Workspace | None = None, out=None):
+    T, k = topk_idx.shape
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    dev = topk_idx.device
+    if out is None:
+        out = (torch.empty(E, dtype=torch.int32, device=dev),
+               torch.empty(E + 1, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev))
+    counts, offsets, sorted_src, dest_of = out
+    need = moe_workspace_size(T, 128, 128, E, k)
+    ws = _ws(ws, need)
+    _check(load_library().moe_permute(_p(topk_idx), T, E, k, _p(counts), _p(offsets),
+                                      _p(sorted_src), _p(dest_of), ws.ptr, ws.nbytes, _stream()),
+           "moe_permute")
+    return counts, offsets, sorted_src, dest_of
+
+
+def moe_grouped_ffn(x, sorted_src, offsets, W1, W3, W2, k: int, y_sorted=None,
+                    ws: Workspace | None = None):
+    T, H = x.shape
+    E, _, F = W1.shape
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    _need(sorted_src, torch.int32, (T * k,), "sorted_src")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    y_sorted = torch.empty(T * k, H, dtype=torch.bfloat16, device=x.device) \
+        if y_sorted is None else y_sorted
+    _need(y_sorted, torch.bfloat16, (T * k, H), "y_sorted")
+    ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    _check(load_library().moe_grouped_ffn(_p(x), _p(sorted_src), _p(offsets), _p(W1), _p(W3),
+                                          _p(W2), T, H, F, E, k, _p(y_sorted), ws.ptr, ws.nbytes,
+                                          _stream()), "moe_grouped_ffn")
+    return y_sorted
+
+
+def moe_combine(y_sorted, dest_of, topk_w, out=None):
+    T, k = topk_w.shape
+    H = y_sorted.shape[1]
+    _need(y_sorted, torch.bfloat16, (y_sorted.shape[0], H), "y_sorted")
+    _need(dest_of, torch.int32, (T * k,), "dest_of")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=y_sorted.device) if out is None else out
+    _need(out, torch.bfloat16, (T, H), "out")
+    _check(load_library().moe_combine(_p(y_sorted), _p(dest_of), _p(topk_w), T, H, k, _p(out),
+                                      _stream()), "moe_combine")
+    return out
+
+
+def moe_forward(x, router_logits, W1, W3, W2, k: int, out=None, ws: Workspace | None = None):
+    T, H = x.shape
+    E, _, F = W1.shape
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_logits, torch.float32, (T, E), "router_logits")
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out, torch.bfloat16, (T, H), "out")
+    ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    _check(load_library().moe_forward(_p(x), _p(router_logits), _p(W1), _p(W3), _p(W2), T, H, F,
+                                      E, k, _p(out), ws.ptr, ws.nbytes, _stream()),
+           "moe_forward")
+    return out
+
+
+FORWARD_STAGES = 7
+
+
+def moe_forward_stage_name(i: int) -> str:
+    r = load_library().moe_forward_stage_name(i)
+    return None if r is None else r.decode()
+
+
+def moe_forward_events(x, router_logits, W1, W3, W2, k: int, events, out=None,
+                       ws: Workspace | None = None):
+    """moe_forward that records events[0] before the first kernel and
+    events[i] after stage i (torch.cuda.Event objects with timing)."""
+    T, H = x.shape
+    E, _, F = W1.shape
+    if len(events) != FORWARD_STAGES + 1:
+        raise ValueError(f"need {FORWARD_STAGES + 1} events")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
+    ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    arr = (ctypes.c_void_p * (FORWARD_STAGES + 1))(*[e.cuda_event for e in events])
+    _check(load_library().moe_forward_events(_p(x), _p(router_logits), _p(W1), _p(W3), _p(W2),
+                                             T, H, F, E, k, _p(out), ws.ptr, ws.nbytes, arr,
+                                             _stream()), "moe_forward_events")
+    return out
+
+
+def moe_forward_host(x_host, logits_host, W1, W3, W2, k: int, out_host=None,
+                     ws: Workspace | None = None):
+    """Host activations in (pinned CPU tensors), host result out; weights on
+    the device.  The result is valid after the current stream synchronises."""
+    T, H = x_host.shape
+    E, _, F = W1.shape
+    _need(x_host, torch.bfloat16, (T, H), "x_host", cuda=False)
+    _need(logits_host, torch.float32, (T, E), "logits_host", cuda=False)
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    out_host = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True) \
+        if out_host is None else out_host
+    _need(out_host, torch.bfloat16, (T, H), "out_host", cuda=False)
+    ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    _check(load_library().moe_forward_host(_p(x_host), _p(logits_host), _p(W1), _p(W3), _p(W2),
+                                           T, H, F, E, k, _p(out_host), ws.ptr, ws.nbytes,
+                                           _stream()), "moe_forward_host")
+    return out_host

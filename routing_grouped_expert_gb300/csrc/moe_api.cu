@@ -1,0 +1,303 @@
+// The extern "C" boundary of libmoe: argument checks, workspace carving and
+// the launch sequence of each entry point.  See include/moe.h for the
+// contract of every call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+int g_is_sm103[kMaxDevices];   // 0 unknown, 1 yes, 2 no
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n > 0 ? n : 1;
+  }
+  return g_sm_count[dev];
+}
+
+bool device_is_sm103() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (g_is_sm103[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_is_sm103[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_is_sm103[dev] == 1;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+bool ok_route_sizes(int T, int E, int k) {
+  return T >= 0 && E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= E && k <= MOE_MAX_TOPK &&
+         (long long)T * k < (1LL << 31) && (long long)T * E < (1LL << 40);
+}
+
+bool ok_sizes(int T, int H, int F, int E, int k) {
+  return ok_route_sizes(T, E, k) && H >= kTileM && F >= kTileM && H % kTileM == 0 &&
+         F % kTileM == 0 && (long long)H * F * E < (1LL << 40);
+}
+
+moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)
+    return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                    \
+  do {                                                   \
+    cudaError_t _e = (expr);                             \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;          \
+  } while (0)
+
+const char* const kStageNames[MOE_FORWARD_STAGES] = {"route", "scan", "scatter", "gather",
+                                                     "fc1", "fc2", "combine"};
+
+// The launch sequence of the whole layer on device buffers.  With `ev`
+// non-null, ev[0] is recorded first and ev[i] after stage i.
+moe_status forward_device(const void* x, const float* logits, const void* W1, const void* W3,
+                          const void* W2, int T, int H, int F, int E, int k, void* out,
+                          void* ws, const WsLayout& L, cudaStream_t s,
+                          const cudaEvent_t* ev = nullptr) {
+  const int P = T * k;
+  const int C = num_chunks(T, k);
+  int* status = ws_ptr<int>(ws, L.status);
+  int32_t* topk_idx = ws_ptr<int32_t>(ws, L.topk_idx);
+  float* topk_w = ws_ptr<float>(ws, L.topk_w);
+  int32_t* counts = ws_ptr<int32_t>(ws, L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(ws, L.offsets);
+  int32_t* sorted_src = ws_ptr<int32_t>(ws, L.sorted_src);
+  int32_t* dest_of = ws_ptr<int32_t>(ws, L.dest_of);
+  int32_t* chunk = ws_ptr<int32_t>(ws, L.chunk_base);
+  int32_t* block_off = ws_ptr<int32_t>(ws, L.block_off);
+  int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
+  int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
+  __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
+  __nv_bfloat16* h = ws_ptr<__nv_bfloat16>(ws, L.h);
+  __nv_bfloat16* y = ws_ptr<__nv_bfloat16>(ws, L.y);
+
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  MOE_TRY(mark(0));
+  MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
+  MOE_TRY(mark(1));
+  MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert, s));
+  MOE_TRY(mark(2));
+  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
+  MOE_TRY(mark(3));
+  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
+  MOE_TRY(mark(4));
+  MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
+                             static_cast<const __nv_bfloat16*>(W1),
+                             static_cast<const __nv_bfloat16*>(W3),
+                             static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
+                             ev ? ev[5] : nullptr));
+  MOE_TRY(mark(6));
+  MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s));
+  MOE_TRY(mark(7));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int H, int F, int E, int k) {
+  if (!ok_sizes(T, H, F, E, k)) return 0;
+  return ws_layout(T, H, F, E, k).total;
+}
+
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                          float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_route_sizes(T, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(logits) || !ok_ptr(topk_idx) || !ok_ptr(topk_w)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256)
+    return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  return cuda_status(launch_route(logits, T, E, k, topk_idx, topk_w, nullptr, status, s));
+}
+
+moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* counts,
+                       int32_t* offsets, int32_t* sorted_src, int32_t* dest_of, void* ws,
+                       size_t ws_bytes, void* stream) {
+  if (!ok_route_sizes(T, E, k)) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(sorted_src) || !ok_ptr(dest_of)))
+    return MOE_ERR_INVALID_ARG;
+  // Only the routing part of the layout is used; H = F = 128 keeps it small.
+  const WsLayout L = ws_layout(T, kTileM, kTileM, E, k);
+  if (check_ws(ws, ws_bytes, L.x_perm) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = ws_ptr<int>(ws, L.status);
+  int32_t* chunk = ws_ptr<int32_t>(ws, L.chunk_base);
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  if (T == 0) {
+    // Empty batch: all counts and offsets are zero.
+    MOE_TRY(cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), s));
+    MOE_TRY(cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * sizeof(int32_t), s));
+    return MOE_OK;
+  }
+  const int C = num_chunks(T, k);
+  MOE_TRY(launch_count(topk_idx, T, E, k, chunk, status, s));
+  MOE_TRY(launch_scan(chunk, C, E, counts, offsets, ws_ptr<int32_t>(ws, L.block_off),
+                      ws_ptr<int32_t>(ws, L.num_blocks), ws_ptr<int32_t>(ws, L.block_expert), s));
+  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32_t* offsets,
+                           const void* W1, const void* W3, const void* W2, int T, int H, int F,
+                           int E, int k, void* y_sorted, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(sorted_src) || !ok_ptr(offsets) || !ok_ptr(W1) || !ok_ptr(W3) ||
+      !ok_ptr(W2) || !ok_ptr(y_sorted))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.stage_x) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int P = T * k;
+  int* status = ws_ptr<int>(ws, L.status);
+  int32_t* block_off = ws_ptr<int32_t>(ws, L.block_off);
+  int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
+  int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
+  __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert, s));
+  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
+  MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
+                             static_cast<const __nv_bfloat16*>(W1),
+                             static_cast<const __nv_bfloat16*>(W3),
+                             static_cast<const __nv_bfloat16*>(W2), P, H, F, E,
+                             ws_ptr<__nv_bfloat16>(ws, L.h),
+                             static_cast<__nv_bfloat16*>(y_sorted), status, s));
+  return MOE_OK;
+}
+
+moe_status moe_combine(const void* y_sorted, const int32_t* dest_of, const float* topk_w, int T,
+                       int H, int k, void* out, void* stream) {
+  if (T < 0 || H < kTileM || H % kTileM != 0 || k < 1 || k > MOE_MAX_TOPK ||
+      (long long)T * k >= (1LL << 31))
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(y_sorted) || !ok_ptr(dest_of) || !ok_ptr(topk_w) || !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_combine(static_cast<const __nv_bfloat16*>(y_sorted), dest_of, topk_w,
+                                    T, H, k, static_cast<__nv_bfloat16*>(out),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(const void* x, const float* router_logits, const void* W1,
+                       const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                       void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_events(const void* x, const float* router_logits, const void* W1,
+                              const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                              void* out, void* ws, size_t ws_bytes, void* const* events,
+                              void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (events == nullptr) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_FORWARD_STAGES; ++i)
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L,
+                        static_cast<cudaStream_t>(stream),
+                        reinterpret_cast<const cudaEvent_t*>(events));
+}
+
+const char* moe_forward_stage_name(int i) {
+  return (i >= 0 && i < MOE_FORWARD_STAGES) ? kStageNames[i] : nullptr;
+}
+
+moe_status moe_forward_host(const void* x_host, const float* logits_host, const void* W1,
+                            const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                            void* out_host, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x_host == nullptr || logits_host == nullptr || out_host == nullptr || !ok_ptr(W1) ||
+      !ok_ptr(W3) || !ok_ptr(W2))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* dx = ws_ptr<void>(ws, L.stage_x);
+  float* dl = ws_ptr<float>(ws, L.stage_logits);
+  void* dout = ws_ptr<void>(ws, L.stage_out);
+  MOE_TRY(cudaMemcpyAsync(dx, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s));
+  MOE_TRY(cudaMemcpyAsync(dl, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice, s));
+  const moe_status st = forward_device(dx, dl, W1, W3, W2, T, H, F, E, k, dout, ws, L, s);
+  if (st != MOE_OK) return st;
+  MOE_TRY(cudaMemcpyAsync(out_host, dout, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(const void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  int word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(word);
+}
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (size, null or misaligned pointer, expert index)";
+    case MOE_ERR_NONFINITE: return "a router logit is NaN or infinite";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case MOE_ERR_WORKSPACE: return "workspace is null, misaligned or too small";
+    case MOE_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case MOE_ERR_UNSUPPORTED: return "the current device is not an sm_103 GPU";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// Internal definitions shared by the libmoe translation units: tile sizes,
+// workspace layout, device status word, small device helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- tiling
+// Token block: at most kBlockRows routed rows of one expert.  Each expert's
+// rows are cut into blocks of kBlockRows, which leaves at most one partial
+// block per expert (MegaFlux, §3.1).  The block is the N side of the expert
+// GEMM tile; the M side is kTileM output features.
+constexpr int kBlockRows = 128;
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;           // one 128-byte swizzle atom of bf16
+constexpr int kRowBox = 32;          // token rows per TMA box of the N operand
+constexpr int kGroupBlocks = 16;     // blocks of one expert rastered together
+
+// Permute chunking: one CTA handles the assignments of kChunkAssign / k
+// consecutive tokens (at most kChunkAssign assignments).
+constexpr int kChunkAssign = 512;
+inline __host__ __device__ int tokens_per_chunk(int k) { return kChunkAssign / k; }
+inline __host__ __device__ int num_chunks(int T, int k) {
+  const int tpc = tokens_per_chunk(k);
+  return (T + tpc - 1) / tpc;
+}
+// Upper bound of the number of token blocks over all experts.
+inline __host__ __device__ long long max_blocks(long long P, int E) {
+  const long long nonempty = P < E ? P : E;
+  return (P + kBlockRows - 1) / kBlockRows + nonempty;
+}
+
+// --------------------------------------------------------- device status
+// ws[0]: first error code seen by any kernel (MOE_OK if none);
+// ws[1]: a detail word (which wait timed out) for diagnostics.
+enum : int { kWaitDetailProducer = 1, kWaitDetailMma = 2, kWaitDetailEpilogue = 3,
+             kWaitDetailDrain = 4 };
+
+__device__ __forceinline__ void set_status(int* status, int code, int detail = 0) {
+  if (atomicCAS(status, 0, code) == 0 && detail) status[1] = detail;
+}
+
+// ------------------------------------------------------ workspace layout
+struct WsLayout {
+  size_t status;        // int32[64]
+  size_t topk_idx;      // int32[P]
+  size_t topk_w;        // f32[P]
+  size_t counts;        // int32[E]
+  size_t offsets;       // int32[E+1]
+  size_t sorted_src;    // int32[P]
+  size_t dest_of;       // int32[P]
+  size_t chunk_base;    // int32[C*E]   per-chunk histograms, then bases
+  size_t block_off;     // int32[E+1]
+  size_t num_blocks;    // int32[1]
+  size_t block_expert;  // int32[max_blocks]
+  size_t x_perm;        // bf16[P*H]
+  size_t h;             // bf16[P*F]
+  size_t y;             // bf16[P*H]
+  size_t stage_x;       // bf16[T*H]   device staging for moe_forward_host
+  size_t stage_logits;  // f32[T*E]
+  size_t stage_out;     // bf16[T*H]
+  size_t total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
+  const size_t P = (size_t)T * k;
+  const size_t C = (size_t)num_chunks(T, k);
+  const size_t NB = (size_t)max_blocks((long long)P, E);
+  WsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
+  L.status = take(64 * 4);
+  L.topk_idx = take(P * 4);
+  L.topk_w = take(P * 4);
+  L.counts = take((size_t)E * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.sorted_src = take(P * 4);
+  L.dest_of = take(P * 4);
+  L.chunk_base = take(C * E * 4);
+  L.block_off = take((size_t)(E + 1) * 4);
+  L.num_blocks = take(4);
+  L.block_expert = take(NB * 4 + 4);
+  L.x_perm = take(P * H * 2);
+  L.h = take(P * F * 2);
+  L.y = take(P * H * 2);
+  L.stage_x = take((size_t)T * H * 2);
+  L.stage_logits = take((size_t)T * E * 4);
+  L.stage_out = take((size_t)T * H * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename Tp>
+inline Tp* ws_ptr(void* ws, size_t off) { return reinterpret_cast<Tp*>((char*)ws + off); }
+
+// ------------------------------------------------------------ launchers
+// Each returns cudaSuccess or the launch error.  All enqueue on `s`.
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                         float* topk_w, int32_t* chunk_hist, int* status, cudaStream_t s);
+cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* chunk_hist,
+                         int* status, cudaStream_t s);
+cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
+                        int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
+                        cudaStream_t s);
+cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
+                           const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
+                           cudaStream_t s);
+cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
+                        int32_t* block_expert, cudaStream_t s);
+cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
+                          __nv_bfloat16* x_perm, cudaStream_t s);
+cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
+                               const int32_t* block_off, const int32_t* num_blocks,
+                               const int32_t* block_expert, const __nv_bfloat16* W1,
+                               const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
+                               int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
+                               cudaStream_t s, cudaEvent_t after_fc1 = nullptr);
+cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
+                           const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
+                           cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+// True when the current device is compute capability 10.3.
+bool device_is_sm103();
+
+}  // namespace moe

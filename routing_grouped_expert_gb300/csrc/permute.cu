@@ -1,0 +1,188 @@
+// Step 2: per-expert counts, exclusive scan, and the stable counting-sort
+// scatter into per-expert groups ("MegaScale-Infer", §3.4 Fused Kernels,
+// steps (2) and (4)).  Inside an expert, assignments a = t*k + j keep
+// ascending a, i.e. order by token then top-k position ("MegaFlux", §A.2).
+//
+// Three kernels, all deterministic (no order-dependent atomics):
+//   count/route : histogram of each chunk of assignments (order-free atomics
+//                 on integers only);
+//   scan        : per-expert prefix over chunks -> each chunk's base position,
+//                 exclusive scan over experts -> offsets, plus the token-block
+//                 plan (blocks of <= 128 rows per expert, "MegaFlux", §3.1);
+//   scatter     : rank of each assignment among equal experts inside its
+//                 chunk (warp match + per-warp counts), base + rank.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// Exclusive scan of one int per thread over a block of kScanThreads threads.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  __syncthreads();   // warp_sums may be in use by a previous call
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += u;
+    }
+    warp_sums[lane] = wi - w;   // exclusive prefix of warp totals
+    if (lane == 31) warp_sums[32] = wi;
+  }
+  __syncthreads();
+  *total = warp_sums[32];
+  return warp_sums[warp] + incl - v;
+}
+
+// counts -> block_off (exclusive prefix of ceil(count / kBlockRows)),
+// num_blocks, and block_expert[b] = expert of block b.
+__device__ __forceinline__ void write_block_plan(int e, int E, int cnt, int32_t* block_off,
+                                                 int32_t* num_blocks, int32_t* block_expert,
+                                                 int* warp_sums) {
+  const int nb = (e < E) ? (cnt + kBlockRows - 1) / kBlockRows : 0;
+  int total_nb;
+  const int boff = block_exclusive_scan(nb, &total_nb, warp_sums);
+  if (e < E) {
+    block_off[e] = boff;
+    for (int b = 0; b < nb; ++b) block_expert[boff + b] = e;
+  }
+  if (threadIdx.x == 0) {
+    block_off[E] = total_nb;
+    *num_blocks = total_nb;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets, int32_t* __restrict__ block_off,
+            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert) {
+  __shared__ int warp_sums[33];
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    // prefix over chunks: chunk c's rows of expert e start after chunks < c
+    for (int c = 0; c < C; ++c) {
+      const int v = chunk_hist[(size_t)c * E + e];
+      chunk_hist[(size_t)c * E + e] = cnt;
+      cnt += v;
+    }
+  }
+  int total;
+  const int off = block_exclusive_scan(e < E ? cnt : 0, &total, warp_sums);
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    for (int c = 0; c < C; ++c) chunk_hist[(size_t)c * E + e] += off;
+  }
+  if (e == 0) offsets[E] = total;
+  write_block_plan(e, E, cnt, block_off, num_blocks, block_expert, warp_sums);
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+plan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ block_off,
+            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert) {
+  __shared__ int warp_sums[33];
+  const int e = threadIdx.x;
+  const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
+  write_block_plan(e, E, cnt, block_off, num_blocks, block_expert, warp_sums);
+}
+
+__global__ void __launch_bounds__(kChunkAssign)
+scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_assign,
+               const int32_t* __restrict__ chunk_base, int32_t* __restrict__ sorted_src,
+               int32_t* __restrict__ dest_of) {
+  extern __shared__ int cnt[];   // [warps][E]
+  const int nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * chunk_assign + threadIdx.x;
+  int e = (threadIdx.x < chunk_assign && a < P) ? topk_idx[a] : -1;
+  if (e >= E) e = -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank_w == 0) cnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int s = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int v = cnt[w * E + x];
+      cnt[w * E + x] = s;
+      s += v;
+    }
+  }
+  __syncthreads();
+  if (e >= 0) {
+    const int pos = chunk_base[(size_t)blockIdx.x * E + e] + cnt[warp * E + e] + rank_w;
+    sorted_src[pos] = a;
+    dest_of[a] = pos;
+  }
+}
+
+// x_perm[p] = x[sorted_src[p] / k]: one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256)
+gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sorted_src, int P,
+              int H, int k, __nv_bfloat16* __restrict__ x_perm) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= P) return;
+  const int t = sorted_src[row] / k;
+  const int4* src = reinterpret_cast<const int4*>(x + (size_t)t * H);
+  int4* dst = reinterpret_cast<int4*>(x_perm + (size_t)row * H);
+  const int nv = H / 8;
+  for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
+}
+
+}  // namespace
+
+cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
+                        int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
+                        cudaStream_t s) {
+  scan_kernel<<<1, kScanThreads, 0, s>>>(chunk_hist, C, E, counts, offsets, block_off,
+                                         num_blocks, block_expert);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
+                        int32_t* block_expert, cudaStream_t s) {
+  plan_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, block_off, num_blocks, block_expert);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
+                           const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int C = num_chunks(T, k);
+  const int chunk_assign = tokens_per_chunk(k) * k;
+  const size_t smem = (size_t)(kChunkAssign / 32) * E * sizeof(int);
+  // 16 warps x E counters; above the default 48 KB when E > 768.
+  cudaError_t err = cudaFuncSetAttribute(
+      scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)((kChunkAssign / 32) * MOE_MAX_EXPERTS * sizeof(int)));
+  if (err != cudaSuccess) return err;
+  scatter_kernel<<<C, kChunkAssign, smem, s>>>(topk_idx, T * k, E, chunk_assign, chunk_base,
+                                               sorted_src, dest_of);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
+                          __nv_bfloat16* x_perm, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  gather_kernel<<<(P + 7) / 8, 256, 0, s>>>(x, sorted_src, P, H, k, x_perm);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,156 @@
+// Step 1: top-k gating and weight normalisation, one warp per token
+// ("MegaScale-Infer", §3.4 Fused Kernels, steps (1) and (3)), fused with
+// the per-chunk expert histogram that step (2) needs.
+//
+// Selection is k rounds of a warp arg-max on the raw fp32 logits: a larger
+// value wins, equal values (IEEE ==, so -0.0 ties +0.0) go to the lower
+// expert index.  The weights are the softmax over the k selected logits,
+// in fp32 with the largest selected logit subtracted first.
+#include <math.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;   // 8 warps, each loops over tokens
+
+struct Cand {
+  float v;
+  int i;   // expert index, -1 = no candidate
+};
+
+// True when candidate b should replace a.
+__device__ __forceinline__ bool better(const Cand& b, const Cand& a) {
+  if (b.i < 0) return false;
+  if (a.i < 0) return true;
+  return b.v > a.v || (b.v == a.v && b.i < a.i);
+}
+
+template <int kPerLane>
+__global__ void __launch_bounds__(kRouteThreads)
+route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int tpc,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                  int32_t* __restrict__ chunk_hist, int* __restrict__ status) {
+  extern __shared__ int hist_s[];   // [E] when chunk_hist != nullptr
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t_begin = blockIdx.x * tpc;
+  const int t_end = min(T, t_begin + tpc);
+  if (chunk_hist) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
+    __syncthreads();
+  }
+  bool nonfinite = false;
+  for (int t = t_begin + warp; t < t_end; t += kRouteThreads / 32) {
+    const float* row = logits + (size_t)t * E;
+    float v[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = lane + 32 * i;
+      float x = (e < E) ? __ldg(row + e) : -INFINITY;
+      if (e < E && !isfinite(x)) {
+        nonfinite = true;
+        if (isnan(x)) x = -INFINITY;   // keep the order total; status reports it
+      }
+      v[i] = x;
+    }
+    uint32_t taken = 0;
+    float my_sel = 0.f;
+    int my_idx = 0;
+    for (int j = 0; j < k; ++j) {
+      Cand c{-INFINITY, -1};
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u)) {
+          Cand d{v[i], e};
+          if (better(d, c)) c = d;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        Cand o{__shfl_xor_sync(0xffffffffu, c.v, off), __shfl_xor_sync(0xffffffffu, c.i, off)};
+        if (better(o, c)) c = o;
+      }
+      if (c.i >= 0 && (c.i & 31) == lane) taken |= 1u << (c.i >> 5);
+      if (lane == j) {
+        my_sel = c.v;
+        my_idx = c.i;
+      }
+    }
+    // softmax over the k selected logits (slot 0 holds the largest)
+    const float m = __shfl_sync(0xffffffffu, my_sel, 0);
+    float ex = (lane < k) ? expf(my_sel - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_idx;
+      topk_w[(size_t)t * k + lane] = ex / sum;
+      if (chunk_hist && my_idx >= 0 && my_idx < E) atomicAdd(&hist_s[my_idx], 1);
+    }
+  }
+  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  if (chunk_hist) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      chunk_hist[(size_t)blockIdx.x * E + e] = hist_s[e];
+  }
+}
+
+// Per-chunk histogram of a caller-supplied topk_idx (moe_permute on its own).
+__global__ void __launch_bounds__(kChunkAssign)
+count_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_assign,
+             int32_t* __restrict__ chunk_hist, int* __restrict__ status) {
+  extern __shared__ int hist_s[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * chunk_assign + threadIdx.x;
+  if (threadIdx.x < chunk_assign && a < P) {
+    const int e = topk_idx[a];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist_s[e], 1);
+    else
+      set_status(status, MOE_ERR_INVALID_ARG);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_hist[(size_t)blockIdx.x * E + e] = hist_s[e];
+}
+
+template <int kPerLane>
+cudaError_t launch_route_t(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                           float* topk_w, int32_t* chunk_hist, int* status, cudaStream_t s) {
+  const int tpc = tokens_per_chunk(k);
+  const int C = num_chunks(T, k);
+  const size_t smem = chunk_hist ? (size_t)E * sizeof(int) : 0;
+  route_topk_kernel<kPerLane><<<C, kRouteThreads, smem, s>>>(logits, T, E, k, tpc, topk_idx,
+                                                             topk_w, chunk_hist, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                         float* topk_w, int32_t* chunk_hist, int* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (E <= 32) return launch_route_t<1>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+  if (E <= 64) return launch_route_t<2>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+  if (E <= 128) return launch_route_t<4>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+  if (E <= 256) return launch_route_t<8>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+  if (E <= 512)
+    return launch_route_t<16>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+  return launch_route_t<32>(logits, T, E, k, topk_idx, topk_w, chunk_hist, status, s);
+}
+
+cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* chunk_hist,
+                         int* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int C = num_chunks(T, k);
+  const int chunk_assign = tokens_per_chunk(k) * k;
+  count_kernel<<<C, kChunkAssign, (size_t)E * sizeof(int), s>>>(topk_idx, T * k, E, chunk_assign,
+                                                                chunk_hist, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

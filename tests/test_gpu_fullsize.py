@@ -1,0 +1,47 @@
+"""The five workloads of record at full size, through moe_forward exactly as
+the benchmark launches it.  Routing and the permutation are compared in full
+(bit-exact); the layer output is compared on sampled tokens that the oracle
+computes one by one from the per-token definition."""
+import numpy as np
+import pytest
+import torch
+
+import routing_grouped_expert_gb300 as moe
+from oracle import moe_oracle as O
+from routing_grouped_expert_gb300 import inputs as I
+from tests.helpers import W_ATOL, assert_moe_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["mixtral_decode", "dbrx_prefill", "fine_grained", "skewed", "skewed_10x"]
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_workload(name):
+    wl = I.WORKLOADS[name]
+    d = I.make_inputs(wl, "cuda")
+    logits_cpu = d["logits"].cpu()
+    # routing and permutation: full arrays, bit-exact
+    idx_ref, w_ref = O.route_topk(logits_cpu.numpy(), wl.k)
+    idx, w = moe.moe_route_topk(d["logits"], wl.k)
+    np.testing.assert_array_equal(to_np(idx), idx_ref)
+    np.testing.assert_allclose(to_np(w), w_ref, rtol=0, atol=W_ATOL)
+    perm_ref = O.permute(idx_ref, wl.E)
+    for got, ref in zip(moe.moe_permute(idx, wl.E), perm_ref):
+        np.testing.assert_array_equal(to_np(got), ref)
+    # the fused layer, twice: bit-reproducible
+    ws = moe.Workspace()
+    out = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k, ws=ws)
+    out2 = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k, ws=ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(out, out2)
+    # sampled tokens against the per-token definition
+    rng = np.random.default_rng(0)
+    tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, 4, replace=False)]))
+    ref = O.forward_direct(d["x"], logits_cpu.numpy(), d["W1"], d["W3"], d["W2"], wl.k,
+                           tokens=tokens)
+    assert_moe_close(out[torch.from_numpy(tokens).cuda()], ref, f"{name} sampled out")
+    # properties that hold at any size
+    counts = to_np(moe.moe_permute(idx, wl.E)[0])
+    assert counts.sum() == wl.T * wl.k
+    assert torch.isfinite(out.float()).all()
