@@ -237,6 +237,9 @@ def moe_forward_events(x, router_logits, W1, W3, W2, k: int, events, out=None,
         raise ValueError(f"need {FORWARD_STAGES + 1} events")
     out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
     ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    for e in events:            # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record()
     arr = (ctypes.c_void_p * (FORWARD_STAGES + 1))(*[e.cuda_event for e in events])
     _check(load_library().moe_forward_events(_p(x), _p(router_logits), _p(W1), _p(W3), _p(W2),
                                              T, H, F, E, k, _p(out), ws.ptr, ws.nbytes, arr,

@@ -1,0 +1,54 @@
+"""The benchmark's multi-rank host logic on CPU ranks (gloo, world size 2):
+the slowest rank's time sets the whole-job throughput, and the reference arm
+runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    local_ms = 100.0 + 50.0 * rank                    # rank 1 is the slow one
+    slowest = bench.max_over_ranks(local_ms, world, torch.device("cpu"))
+    value = bench.throughput(world, 128, 10, slowest)
+    ref = bench.bench_reference(None, rank, world, 0) if rank != 0 else "skipped"
+    q.put((rank, slowest, value, ref))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, slowest, value, ref in got:
+        assert slowest == 150.0
+        assert value == pytest.approx(2 * 128 * 10 / 0.150)
+    assert got[1][3] is None        # the reference arm does no work off rank 0
+
+
+def test_single_rank_throughput():
+    import bench
+    assert bench.max_over_ranks(3.5, 1, None) == 3.5
+    assert bench.throughput(1, 128, 500, 400.0) == pytest.approx(128 * 500 / 0.4)
