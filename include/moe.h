@@ -131,6 +131,46 @@ moe_status moe_combine(const void* y_sorted, const int32_t* dest_of,
                        void* out, void* stream);
 
 /*
+ * moe_permute for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for how the library is
+ * called, not for what the layer computes.
+ *
+ * Who needs it: code whose device memory is wholly owned by another
+ * allocator (a serving engine or host framework that reserves the GPU's
+ * memory up front and hands out no extra buffers), and code on a hot path
+ * that must not take cudaMalloc's implicit device synchronisation.  Such a
+ * caller cannot provide the workspace moe_permute needs, so this variant
+ * takes none and performs no allocation of any kind (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ * Arguments, outputs and ordering are those of moe_permute.  Its scratch
+ * (per-chunk histograms, the token-block plan, a status word) is a fixed
+ * device array of MOE_PERMUTE_NOALLOC_SCRATCH_BYTES inside the library;
+ * every GPU on which the library's device code is loaded holds that array
+ * until the process exits.  Sizes whose scratch would not fit return
+ * MOE_ERR_WORKSPACE and enqueue nothing; they fit while
+ *   4 * (64 + C*E + (E+1) + 64 + NB) <= MOE_PERMUTE_NOALLOC_SCRATCH_BYTES
+ * (each term rounded up to 64), with C = ceil(T / floor(512 / k)) chunks
+ * and NB = ceil(T*k / 128) + min(T*k, E) token blocks -- for example
+ * T = 8192, k = 8, E = 256 needs about 136 KB.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture begins.  Every call shares the one array and
+ * it keeps the previous call's contents (the status word is cleared by
+ * each call), so calls whose work overlaps on the GPU -- on different
+ * streams, or from different threads -- race and corrupt each other's
+ * results; serialise them.  Out-of-range expert indices are skipped (the
+ * outputs are then unspecified) but, unlike moe_permute, cannot be read
+ * back as a device status.
+ */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int E, int k,
+                               int32_t* counts, int32_t* offsets,
+                               int32_t* sorted_src, int32_t* dest_of,
+                               void* stream);
+
+/*
  * The whole layer: steps 1-4 on `stream`, intermediates in `ws`.
  *   x [T, H] bf16, router_logits [T, E] fp32, W1/W3 [E, H, F] bf16,
  *   W2 [E, F, H] bf16, out [T, H] bf16.

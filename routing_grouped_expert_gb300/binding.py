@@ -24,6 +24,7 @@ SIGNATURES = {
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_route_topk": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP]),
     "moe_permute": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_permute_noalloc": (_I, [_VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
     "moe_grouped_ffn": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ,
                              _VP]),
     "moe_combine": (_I, [_VP, _VP, _VP, _I, _I, _I, _VP, _VP]),
