@@ -1,9 +1,9 @@
 // Step 4: weighted return to token order, the final top-k sum
 // ("MegaFlux", §2.1; "MegaScale-Infer", §3.2 step (4)):
 //   out[t] = sum_{j<k} topk_w[t,j] * y_sorted[dest_of[t*k+j]]
-// One CTA per token; each thread owns 8 consecutive columns (one 16-byte
-// vector) and sums the k expert rows in slot order in fp32, so the result
-// is bit-identical run to run.
+// One CTA per (token, 1024-column slice); each thread owns 8 consecutive
+// columns (one 16-byte vector) and sums the k expert rows in slot order in
+// fp32, so the result is bit-identical run to run.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -27,14 +27,15 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
                __nv_bfloat16* __restrict__ out) {
   __shared__ int s_row[MOE_MAX_TOPK];
   __shared__ float s_w[MOE_MAX_TOPK];
-  const int t = blockIdx.x;
+  const int t = blockIdx.y;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = dest_of[(size_t)t * k + threadIdx.x];
     s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
   const int nv = H / 8;
-  for (int v = threadIdx.x; v < nv; v += kCombineThreads) {
+  for (int v = blockIdx.x * kCombineThreads + threadIdx.x; v < nv;
+       v += gridDim.x * kCombineThreads) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -61,7 +62,9 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k, out);
+  const int slices = (H / 8 + kCombineThreads - 1) / kCombineThreads;
+  combine_kernel<<<dim3(slices, T), kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k,
+                                                            out);
   return cudaGetLastError();
 }
 

@@ -37,25 +37,32 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = kTileM;          // features per tile (MMA M)
-constexpr int BN = kBlockRows;      // max token rows per tile (MMA N)
+constexpr int BM = kTileM;          // weight rows (output features) per MMA (M)
 constexpr int BK = kTileK;          // K per pipeline stage
 constexpr int kAHalfBytes = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
-constexpr int kABytes = BM * BK * 2;              // 16 KB
+constexpr int kABytes = BM * BK * 2;              // 16 KB per weight tile per stage
 constexpr int kBBoxBytes = kRowBox * BK * 2;      // 32 token rows: 4 KB
-constexpr int kBBytes = BN * BK * 2;              // 16 KB
 constexpr int kThreads = 192;
+constexpr int kSmemBudget = 196608;               // operand ring: 192 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
-template <bool kGLU>
+// kNumA weight tiles of 128 rows share each token block:
+//   FC1 (kGLU): gate and up tiles of the same 128 features;
+//   FC2 with kNumA = 2: two adjacent 128-feature tiles of W2.
+// kBN = token rows per block (beta), kAccBufs = TMEM accumulator buffers.
+template <int kNumA, bool kGLU, int kBN, int kAccBufs>
 struct Cfg {
-  static constexpr int kNumA = kGLU ? 2 : 1;
+  static constexpr int kBBytes = kBN * BK * 2;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
-  static constexpr int kStages = kGLU ? 4 : 6;
-  static constexpr int kAccCols = kNumA * BN;          // fp32 columns per accumulator
-  static constexpr int kTmemCols = 2 * kAccCols;       // double-buffered
+  static constexpr int kStages = kSmemBudget / kStageBytes;
+  static constexpr int kAccCols = kNumA * kBN;            // fp32 columns per buffer
+  static constexpr int kTmemCols = kAccBufs * kAccCols;
+  static constexpr int kFeatPerItem = kGLU ? BM : kNumA * BM;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+  static_assert(kStages >= 2 && kStages <= 8, "stages");
+  static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
 };
 
 struct Bars {
@@ -74,6 +81,7 @@ struct Item {
 };
 
 // Flat tile index -> (expert, first row, rows, feature tile).
+template <int kBN>
 __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* block_expert,
                                             const int32_t* block_off, const int32_t* offsets) {
   const int q = w / n_mt;                 // some block of the tile's expert
@@ -90,12 +98,12 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   Item it;
   it.e = e;
   it.mt = mt;
-  it.row0 = offsets[e] + b * BN;
-  it.nrows = min(BN, offsets[e + 1] - it.row0);
+  it.row0 = offsets[e] + b * kBN;
+  it.nrows = min(kBN, offsets[e + 1] - it.row0);
   return it;
 }
 
-template <bool kGLU>
+template <int kNumA, bool kGLU, int kBN, int kAccBufs>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -104,7 +112,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
                     __nv_bfloat16* __restrict__ out, int ld_out, int* __restrict__ status) {
-  using C = Cfg<kGLU>;
+  using C = Cfg<kNumA, kGLU, kBN, kAccBufs>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -118,7 +126,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&bars->acc_full[b], 1);
       mbar_init(&bars->acc_empty[b], 4);   // one arrival per epilogue warp
     }
@@ -144,31 +152,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();   // weights: streamed
+      // Weights: with 128-row blocks (decode-like layers) each weight tile has
+      // one consumer and is streamed past L2; with 256-row blocks the sibling
+      // blocks of an expert read the same tile moments later, so it stays.
+      const uint64_t pol_w =
+          (kBN == kBlockRowsLarge) ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();    // token rows: reused
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const Item it = decode_item(w, n_mt, block_expert, block_off, offsets);
+        const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
-        const uint32_t bytes = C::kNumA * kABytes + nbox * kBBoxBytes;
-        const int f0 = it.mt * BM;
+        const uint32_t bytes = kNumA * kABytes + nbox * kBBoxBytes;
+        const int f0 = it.mt * C::kFeatPerItem;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           uint8_t* sA = smem + stage * C::kStageBytes;
-          uint8_t* sB = sA + C::kNumA * kABytes;
+          uint8_t* sB = sA + kNumA * kABytes;
           uint64_t* fb = &bars->full[stage];
           const int k0 = kb * BK;
           mbar_arrive_expect_tx(fb, bytes);
-          tma_load_3d(sA, &tmA0, fb, f0, k0, it.e, pol_w);
-          tma_load_3d(sA + kAHalfBytes, &tmA0, fb, f0 + 64, k0, it.e, pol_w);
-          if constexpr (kGLU) {
-            tma_load_3d(sA + kABytes, &tmA1, fb, f0, k0, it.e, pol_w);
-            tma_load_3d(sA + kABytes + kAHalfBytes, &tmA1, fb, f0 + 64, k0, it.e, pol_w);
+#pragma unroll
+          for (int a = 0; a < kNumA; ++a) {
+            const CUtensorMap* map = (kGLU && a == 1) ? &tmA1 : &tmA0;
+            const int fa = f0 + (kGLU ? 0 : a * BM);
+            tma_load_3d(sA + a * kABytes, map, fb, fa, k0, it.e, pol_w);
+            tma_load_3d(sA + a * kABytes + kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
           }
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(sB + bx * kBBoxBytes, &tmB, fb, k0, it.row0 + bx * kRowBox, pol_x);
@@ -196,7 +209,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const Item it = decode_item(w, n_mt, block_expert, block_off, offsets);
+        const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int n = (it.nrows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n, /*a_mn=*/true, /*b_mn=*/false);
         if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -212,7 +225,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           }
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
-          const uint32_t b0 = a0 + (uint32_t)(C::kNumA * kABytes);
+          const uint32_t b0 = a0 + (uint32_t)(kNumA * kABytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
@@ -220,9 +233,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             const uint64_t db = sdesc_sw128(b0 + kk * 32, 16, 1024);
             // M operand: MN-major; 64-feature atoms 8 KB apart (LBO), 8 K-rows
             // per 1 KB group (SBO); K step of 16 = 16 rows = 2 KB.
-            mma_bf16_ss(d0, sdesc_sw128(a0 + kk * 2048, kAHalfBytes, 1024), db, idesc, accum);
-            if constexpr (kGLU)
-              mma_bf16_ss(d0 + BN, sdesc_sw128(a0 + kABytes + kk * 2048, kAHalfBytes, 1024), db,
+#pragma unroll
+            for (int a = 0; a < kNumA; ++a)
+              mma_bf16_ss(d0 + (uint32_t)(a * kBN),
+                          sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024), db,
                           idesc, accum);
           }
           mma_commit(&bars->empty[stage]);
@@ -233,7 +247,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
         if (!ok) break;
         mma_commit(&bars->acc_full[acc]);
-        if (++acc == 2) {
+        if (++acc == kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -254,14 +268,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      const Item it = decode_item(w, n_mt, block_expert, block_off, offsets);
+      const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
       const bool got = mbar_wait(&bars->acc_full[acc], acc_phase, abort_flag, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int feat = it.mt * BM + q * 32 + lane;
+      const int feat = it.mt * C::kFeatPerItem + q * 32 + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       __nv_bfloat16* col = out + (size_t)it.row0 * ld_out + feat;
       for (int c0 = 0; c0 < it.nrows; c0 += 16) {
@@ -269,14 +283,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_ld_32x32b_x16(tb + c0, g);
         if constexpr (kGLU) {
           uint32_t u[16];
-          tmem_ld_32x32b_x16(tb + BN + c0, u);
+          tmem_ld_32x32b_x16(tb + kBN + c0, u);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             if (c0 + c < it.nrows) {
               const float gv = __uint_as_float(g[c]);
-              const float hv = gv / (1.0f + __expf(-gv)) * __uint_as_float(u[c]);
+              const float hv = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
               col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(hv);
+            }
+          }
+        } else if constexpr (kNumA == 2) {
+          uint32_t g2[16];
+          tmem_ld_32x32b_x16(tb + kBN + c0, g2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c0 + c < it.nrows) {
+              col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(__uint_as_float(g[c]));
+              col[(size_t)(c0 + c) * ld_out + BM] = __float2bfloat16_rn(__uint_as_float(g2[c]));
             }
           }
         } else {
@@ -290,7 +315,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
-      if (++acc == 2) {
+      if (++acc == kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -339,25 +364,49 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGLU>
+template <int kNumA, bool kGLU, int kBN, int kAccBufs>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const int32_t* offsets, const int32_t* block_off,
-                        const int32_t* num_blocks, const int32_t* block_expert, int n_mt, int K,
-                        long long nb_max, __nv_bfloat16* out, int ld_out, int* status,
+                        const int32_t* num_blocks, const int32_t* block_expert, int M_total,
+                        int K, long long nb_max, __nv_bfloat16* out, int ld_out, int* status,
                         cudaStream_t s) {
-  using C = Cfg<kGLU>;
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kGLU>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  using C = Cfg<kNumA, kGLU, kBN, kAccBufs>;
+  auto kern = grouped_gemm_kernel<kNumA, kGLU, kBN, kAccBufs>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
+  const int n_mt = M_total / C::kFeatPerItem;
   const long long items = nb_max * n_mt;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  grouped_gemm_kernel<kGLU><<<grid, kThreads, C::kSmemBytes, s>>>(
-      a0, a1, b, offsets, block_off, num_blocks, block_expert, n_mt, K, out, ld_out, status);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, offsets, block_off, num_blocks,
+                                             block_expert, n_mt, K, out, ld_out, status);
   return cudaGetLastError();
 }
 
+// Tile configuration of a layer: decode-like layers (at most 128 routed rows
+// per expert on average) keep 128-row blocks and double-buffered
+// accumulators so a tile's epilogue overlaps the next tile's weight stream;
+// larger layers use 256-row blocks and two 128-row weight tiles per CTA
+// tile, which halves the operand bytes each SM pulls from L2 per FLOP.
+enum class FfnMode { kSmall, kLarge };
+
+FfnMode ffn_mode(int P, int E) { return (P <= kBlockRows * (long long)E) ? FfnMode::kSmall
+                                                                          : FfnMode::kLarge; }
+
+// FC2 pairs two W2 tiles when H allows it and K is long enough that the
+// single-buffered epilogue is a small share of a tile.
+#ifndef MOE_FC2_PAIR_MIN_F
+#define MOE_FC2_PAIR_MIN_F 0
+#endif
+bool fc2_paired(int H, int F) { return H % (2 * BM) == 0 && F >= MOE_FC2_PAIR_MIN_F; }
+
 }  // namespace
+
+int ffn_block_rows(int P, int E, int H, int F) {
+  (void)H;
+  (void)F;
+  return ffn_mode(P, E) == FfnMode::kSmall ? kBlockRows : kBlockRowsLarge;
+}
 
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                const int32_t* block_off, const int32_t* num_blocks,
@@ -381,13 +430,27 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
       !make_map(&mW2, W2, 3, dW2, sW2, boxW) || !make_map(&mX, x_perm, 2, dX, sX, boxRows) ||
       !make_map(&mH, h, 2, dH, sH, boxRows))
     return cudaErrorInvalidValue;
-  const long long nb_max = max_blocks(P, E);
-  cudaError_t err = launch_gemm<true>(mW1, mW3, mX, offsets, block_off, num_blocks, block_expert,
-                                      F / BM, H, nb_max, h, F, status, s);
+  cudaError_t err;
+  if (ffn_mode(P, E) == FfnMode::kSmall) {
+    const long long nb_max = max_blocks(P, E, kBlockRows);
+    err = launch_gemm<2, true, kBlockRows, 2>(mW1, mW3, mX, offsets, block_off, num_blocks,
+                                              block_expert, F, H, nb_max, h, F, status, s);
+    if (err != cudaSuccess) return err;
+    if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
+    return launch_gemm<1, false, kBlockRows, 2>(mW2, mW2, mH, offsets, block_off, num_blocks,
+                                                block_expert, H, F, nb_max, y, H, status, s);
+  }
+  const long long nb_max = max_blocks(P, E, kBlockRowsLarge);
+  err = launch_gemm<2, true, kBlockRowsLarge, 1>(mW1, mW3, mX, offsets, block_off, num_blocks,
+                                                 block_expert, F, H, nb_max, h, F, status, s);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
-  return launch_gemm<false>(mW2, mW2, mH, offsets, block_off, num_blocks, block_expert, H / BM,
-                            F, nb_max, y, H, status, s);
+  if (fc2_paired(H, F))
+    return launch_gemm<2, false, kBlockRowsLarge, 1>(mW2, mW2, mH, offsets, block_off,
+                                                     num_blocks, block_expert, H, F, nb_max, y,
+                                                     H, status, s);
+  return launch_gemm<1, false, kBlockRowsLarge, 2>(mW2, mW2, mH, offsets, block_off, num_blocks,
+                                                   block_expert, H, F, nb_max, y, H, status, s);
 }
 
 }  // namespace moe

@@ -97,11 +97,14 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   __nv_bfloat16* y = ws_ptr<__nv_bfloat16>(ws, L.y);
 
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
-  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  // status word and the chunk histogram table (adjacent) start at zero
+  MOE_TRY(cudaMemsetAsync(status, 0, L.chunk_base - L.status + (size_t)C * E * sizeof(int32_t),
+                          s));
   MOE_TRY(mark(0));
   MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
   MOE_TRY(mark(1));
-  MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert, s));
+  MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
+                      ffn_block_rows(P, E, H, F), s));
   MOE_TRY(mark(2));
   MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
   MOE_TRY(mark(3));
@@ -165,7 +168,8 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* co
   const int C = num_chunks(T, k);
   MOE_TRY(launch_count(topk_idx, T, E, k, chunk, status, s));
   MOE_TRY(launch_scan(chunk, C, E, counts, offsets, ws_ptr<int32_t>(ws, L.block_off),
-                      ws_ptr<int32_t>(ws, L.num_blocks), ws_ptr<int32_t>(ws, L.block_expert), s));
+                      ws_ptr<int32_t>(ws, L.num_blocks), ws_ptr<int32_t>(ws, L.block_expert),
+                      kBlockRows, s));
   MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
   return MOE_OK;
 }
@@ -190,7 +194,8 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
   __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
   MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
-  MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert, s));
+  MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert,
+                      ffn_block_rows(P, E, H, F), s));
   MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),

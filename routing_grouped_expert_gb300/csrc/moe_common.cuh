@@ -12,11 +12,14 @@
 namespace moe {
 
 // ---------------------------------------------------------------- tiling
-// Token block: at most kBlockRows routed rows of one expert.  Each expert's
-// rows are cut into blocks of kBlockRows, which leaves at most one partial
-// block per expert (MegaFlux, §3.1).  The block is the N side of the expert
-// GEMM tile; the M side is kTileM output features.
+// Token block: at most beta routed rows of one expert.  Each expert's rows
+// are cut into blocks of beta rows, which leaves at most one partial block
+// per expert (MegaFlux, §3.1).  The block is the N side of the expert GEMM
+// tile; the M side is kTileM output features.  beta is 128 when experts get
+// few rows (decode batches) and 256 otherwise; kBlockRows is the smaller one
+// and bounds the number of blocks.
 constexpr int kBlockRows = 128;
+constexpr int kBlockRowsLarge = 256;
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;           // one 128-byte swizzle atom of bf16
 constexpr int kRowBox = 32;          // token rows per TMA box of the N operand
@@ -31,9 +34,9 @@ inline __host__ __device__ int num_chunks(int T, int k) {
   return (T + tpc - 1) / tpc;
 }
 // Upper bound of the number of token blocks over all experts.
-inline __host__ __device__ long long max_blocks(long long P, int E) {
+inline __host__ __device__ long long max_blocks(long long P, int E, int beta = kBlockRows) {
   const long long nonempty = P < E ? P : E;
-  return (P + kBlockRows - 1) / kBlockRows + nonempty;
+  return (P + beta - 1) / beta + nonempty;
 }
 
 // --------------------------------------------------------- device status
@@ -78,13 +81,13 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
   L.status = take(64 * 4);
+  L.chunk_base = take(C * E * 4);   // right after the status: one memset clears both
   L.topk_idx = take(P * 4);
   L.topk_w = take(P * 4);
   L.counts = take((size_t)E * 4);
   L.offsets = take((size_t)(E + 1) * 4);
   L.sorted_src = take(P * 4);
   L.dest_of = take(P * 4);
-  L.chunk_base = take(C * E * 4);
   L.block_off = take((size_t)(E + 1) * 4);
   L.num_blocks = take(4);
   L.block_expert = take(NB * 4 + 4);
@@ -109,12 +112,15 @@ cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* 
                          int* status, cudaStream_t s);
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
-                        cudaStream_t s);
+                        int beta, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
                            cudaStream_t s);
 cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
-                        int32_t* block_expert, cudaStream_t s);
+                        int32_t* block_expert, int beta, cudaStream_t s);
+// Token-block rows (beta) the grouped FFN uses for a layer of these sizes;
+// the block plan must be built with the same value.
+int ffn_block_rows(int P, int E, int H, int F);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s);
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,

@@ -46,12 +46,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp
   return warp_sums[warp] + incl - v;
 }
 
-// counts -> block_off (exclusive prefix of ceil(count / kBlockRows)),
+// counts -> block_off (exclusive prefix of ceil(count / beta)),
 // num_blocks, and block_expert[b] = expert of block b.
-__device__ __forceinline__ void write_block_plan(int e, int E, int cnt, int32_t* block_off,
-                                                 int32_t* num_blocks, int32_t* block_expert,
-                                                 int* warp_sums) {
-  const int nb = (e < E) ? (cnt + kBlockRows - 1) / kBlockRows : 0;
+__device__ __forceinline__ void write_block_plan(int e, int E, int cnt, int beta,
+                                                 int32_t* block_off, int32_t* num_blocks,
+                                                 int32_t* block_expert, int* warp_sums) {
+  const int nb = (e < E) ? (cnt + beta - 1) / beta : 0;
   int total_nb;
   const int boff = block_exclusive_scan(nb, &total_nb, warp_sums);
   if (e < E) {
@@ -67,7 +67,7 @@ __device__ __forceinline__ void write_block_plan(int e, int E, int cnt, int32_t*
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict__ counts,
             int32_t* __restrict__ offsets, int32_t* __restrict__ block_off,
-            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert) {
+            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta) {
   __shared__ int warp_sums[33];
   const int e = threadIdx.x;
   int cnt = 0;
@@ -87,16 +87,16 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict_
     for (int c = 0; c < C; ++c) chunk_hist[(size_t)c * E + e] += off;
   }
   if (e == 0) offsets[E] = total;
-  write_block_plan(e, E, cnt, block_off, num_blocks, block_expert, warp_sums);
+  write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
 }
 
 __global__ void __launch_bounds__(kScanThreads)
 plan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ block_off,
-            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert) {
+            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta) {
   __shared__ int warp_sums[33];
   const int e = threadIdx.x;
   const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
-  write_block_plan(e, E, cnt, block_off, num_blocks, block_expert, warp_sums);
+  write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
 }
 
 __global__ void __launch_bounds__(kChunkAssign)
@@ -131,33 +131,37 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_ass
   }
 }
 
-// x_perm[p] = x[sorted_src[p] / k]: one warp per row, 16-byte vectors.
+// x_perm[p] = x[sorted_src[p] / k], 16-byte vectors, grid-stride over all
+// vectors of all rows so every SM takes part.
 __global__ void __launch_bounds__(256)
 gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sorted_src, int P,
               int H, int k, __nv_bfloat16* __restrict__ x_perm) {
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= P) return;
-  const int t = sorted_src[row] / k;
-  const int4* src = reinterpret_cast<const int4*>(x + (size_t)t * H);
-  int4* dst = reinterpret_cast<int4*>(x_perm + (size_t)row * H);
   const int nv = H / 8;
-  for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
+  const long long total = (long long)P * nv;
+  const int4* src = reinterpret_cast<const int4*>(x);
+  int4* dst = reinterpret_cast<int4*>(x_perm);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(i / nv);
+    const int v = (int)(i - (long long)row * nv);
+    const int t = __ldg(sorted_src + row) / k;
+    dst[i] = __ldg(src + (size_t)t * nv + v);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
-                        cudaStream_t s) {
+                        int beta, cudaStream_t s) {
   scan_kernel<<<1, kScanThreads, 0, s>>>(chunk_hist, C, E, counts, offsets, block_off,
-                                         num_blocks, block_expert);
+                                         num_blocks, block_expert, beta);
   return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
-                        int32_t* block_expert, cudaStream_t s) {
-  plan_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, block_off, num_blocks, block_expert);
+                        int32_t* block_expert, int beta, cudaStream_t s) {
+  plan_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, block_off, num_blocks, block_expert, beta);
   return cudaGetLastError();
 }
 
@@ -181,7 +185,10 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  gather_kernel<<<(P + 7) / 8, 256, 0, s>>>(x, sorted_src, P, H, k, x_perm);
+  const long long vectors = (long long)P * (H / 8);
+  const long long want = (vectors + 255) / 256;
+  const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
+  gather_kernel<<<grid, 256, 0, s>>>(x, sorted_src, P, H, k, x_perm);
   return cudaGetLastError();
 }
 

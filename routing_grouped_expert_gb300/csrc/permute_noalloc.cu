@@ -82,7 +82,8 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int E,
     return MOE_OK;
   }
   if (moe::launch_count(topk_idx, T, E, k, chunk, status, s) != cudaSuccess ||
-      moe::launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert, s) !=
+      moe::launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
+                       moe::kBlockRows, s) !=
           cudaSuccess ||
       moe::launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s) != cudaSuccess)
     return MOE_ERR_CUDA;

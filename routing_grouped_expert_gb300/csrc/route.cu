@@ -1,6 +1,7 @@
 // Step 1: top-k gating and weight normalisation, one warp per token
 // ("MegaScale-Infer", §3.4 Fused Kernels, steps (1) and (3)), fused with
-// the per-chunk expert histogram that step (2) needs.
+// the per-chunk expert histogram that step (2) needs (integer atomic adds
+// into a zeroed table, so the counts do not depend on their order).
 //
 // Selection is k rounds of a warp arg-max on the raw fp32 logits: a larger
 // value wins, equal values (IEEE ==, so -0.0 ties +0.0) go to the lower
@@ -13,7 +14,7 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;   // 8 warps, each loops over tokens
+constexpr int kRouteThreads = 256;   // 8 warps, one token each
 
 struct Cand {
   float v;
@@ -32,70 +33,60 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int tpc,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                   int32_t* __restrict__ chunk_hist, int* __restrict__ status) {
-  extern __shared__ int hist_s[];   // [E] when chunk_hist != nullptr
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t_begin = blockIdx.x * tpc;
-  const int t_end = min(T, t_begin + tpc);
-  if (chunk_hist) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
-    __syncthreads();
-  }
+  const int t = blockIdx.x * (kRouteThreads / 32) + warp;   // one token per warp
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * E;
   bool nonfinite = false;
-  for (int t = t_begin + warp; t < t_end; t += kRouteThreads / 32) {
-    const float* row = logits + (size_t)t * E;
-    float v[kPerLane];
+  float v[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int e = lane + 32 * i;
+    float x = (e < E) ? __ldg(row + e) : -INFINITY;
+    if (e < E && !isfinite(x)) {
+      nonfinite = true;
+      if (isnan(x)) x = -INFINITY;   // keep the order total; status reports it
+    }
+    v[i] = x;
+  }
+  uint32_t taken = 0;
+  float my_sel = 0.f;
+  int my_idx = 0;
+  for (int j = 0; j < k; ++j) {
+    Cand c{-INFINITY, -1};
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
       const int e = lane + 32 * i;
-      float x = (e < E) ? __ldg(row + e) : -INFINITY;
-      if (e < E && !isfinite(x)) {
-        nonfinite = true;
-        if (isnan(x)) x = -INFINITY;   // keep the order total; status reports it
-      }
-      v[i] = x;
-    }
-    uint32_t taken = 0;
-    float my_sel = 0.f;
-    int my_idx = 0;
-    for (int j = 0; j < k; ++j) {
-      Cand c{-INFINITY, -1};
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u)) {
-          Cand d{v[i], e};
-          if (better(d, c)) c = d;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        Cand o{__shfl_xor_sync(0xffffffffu, c.v, off), __shfl_xor_sync(0xffffffffu, c.i, off)};
-        if (better(o, c)) c = o;
-      }
-      if (c.i >= 0 && (c.i & 31) == lane) taken |= 1u << (c.i >> 5);
-      if (lane == j) {
-        my_sel = c.v;
-        my_idx = c.i;
+      if (e < E && !((taken >> i) & 1u)) {
+        Cand d{v[i], e};
+        if (better(d, c)) c = d;
       }
     }
-    // softmax over the k selected logits (slot 0 holds the largest)
-    const float m = __shfl_sync(0xffffffffu, my_sel, 0);
-    float ex = (lane < k) ? expf(my_sel - m) : 0.f;
-    float sum = ex;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_idx;
-      topk_w[(size_t)t * k + lane] = ex / sum;
-      if (chunk_hist && my_idx >= 0 && my_idx < E) atomicAdd(&hist_s[my_idx], 1);
+    for (int off = 16; off > 0; off >>= 1) {
+      Cand o{__shfl_xor_sync(0xffffffffu, c.v, off), __shfl_xor_sync(0xffffffffu, c.i, off)};
+      if (better(o, c)) c = o;
     }
+    if (c.i >= 0 && (c.i & 31) == lane) taken |= 1u << (c.i >> 5);
+    if (lane == j) {
+      my_sel = c.v;
+      my_idx = c.i;
+    }
+  }
+  // softmax over the k selected logits (slot 0 holds the largest)
+  const float m = __shfl_sync(0xffffffffu, my_sel, 0);
+  float ex = (lane < k) ? expf(my_sel - m) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_idx;
+    topk_w[(size_t)t * k + lane] = ex / sum;
+    // integer counts: the order of the atomic adds does not change them
+    if (chunk_hist && my_idx >= 0 && my_idx < E)
+      atomicAdd(&chunk_hist[(size_t)(t / tpc) * E + my_idx], 1);
   }
   if (__any_sync(0xffffffffu, nonfinite) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
-  if (chunk_hist) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      chunk_hist[(size_t)blockIdx.x * E + e] = hist_s[e];
-  }
 }
 
 // Per-chunk histogram of a caller-supplied topk_idx (moe_permute on its own).
@@ -118,14 +109,15 @@ count_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_assig
     chunk_hist[(size_t)blockIdx.x * E + e] = hist_s[e];
 }
 
+// chunk_hist, when given, must hold zeros: the kernel adds each chunk's
+// per-expert counts into it.
 template <int kPerLane>
 cudaError_t launch_route_t(const float* logits, int T, int E, int k, int32_t* topk_idx,
                            float* topk_w, int32_t* chunk_hist, int* status, cudaStream_t s) {
   const int tpc = tokens_per_chunk(k);
-  const int C = num_chunks(T, k);
-  const size_t smem = chunk_hist ? (size_t)E * sizeof(int) : 0;
-  route_topk_kernel<kPerLane><<<C, kRouteThreads, smem, s>>>(logits, T, E, k, tpc, topk_idx,
-                                                             topk_w, chunk_hist, status);
+  const int warps = kRouteThreads / 32;
+  route_topk_kernel<kPerLane><<<(T + warps - 1) / warps, kRouteThreads, 0, s>>>(
+      logits, T, E, k, tpc, topk_idx, topk_w, chunk_hist, status);
   return cudaGetLastError();
 }
 
