@@ -17,6 +17,7 @@ bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -74,6 +75,21 @@ def load_peaks():
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu
+    record, or None when there is none or the kernel's sources changed since
+    the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[f"{workload}:{kernel}"]
+        blob = b"".join(open(os.path.join(ROOT, p), "rb").read() for p in rec["sources"])
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha256(blob).hexdigest() != rec["source_sha256"]:
+        return None
+    return int(rec["bytes_per_launch"])
 
 
 def wl_config(wl, extra=None):
@@ -304,7 +320,7 @@ def bench_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
         peak_note = f"hbm_gbs ({peak_src})"
-    roof.update({"traffic": None, "kernel": top,
+    roof.update({"traffic": measured_traffic(wl.name, top), "kernel": top,
                  "algorithmic_bytes": kbytes.get(top), "algorithmic_flops": kflops.get(top),
                  "kernel_ms": round(mean_ms[top], 5), "peak_source": peak_note})
 
