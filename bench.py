@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default="mixtral_decode", choices=sorted(I.WORKLOADS))
     ap.add_argument("--shape", default=None,
                     help="T,H,F,E,k: a uniform-routing workload of these sizes instead")
+    ap.add_argument("--sweep", action="store_true",
+                    help="tokens-per-expert sweep of the workload's shape (own JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -450,8 +452,72 @@ def bench_reference(args, rank, world, local):
                     "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------ tokens-per-expert sweep
+def bench_sweep(args):
+    """Expert-layer time against tokens per expert b_e = T*k/E for the
+    workload's (H, F, E, k), with a least-squares fit of the linear expert
+    time model Te = k3 * b_e + k4 ("MegaScale-Infer", §3.4 Performance
+    Simulation Model) and the utilisation model util = min(k/E * B/F * b, 1)
+    ("MegaScale-Infer", §2) evaluated with the measured peaks."""
+    import routing_grouped_expert_gb300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    base = I.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    W1, W3, W2 = I.make_weights(base, dev)
+    ws = moe.Workspace(dev)
+    nst = moe.FORWARD_STAGES
+    points = []
+    for be in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048):
+        T = max(1, be * base.E // base.k)
+        wl = base.with_(T=T, name=f"{base.name}_be{be}")
+        x = I.make_x(wl, dev)
+        logits = I.make_logits(wl).to(dev)
+        out = torch.empty(T, base.H, dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            moe.moe_forward(x, logits, W1, W3, W2, base.k, out=out, ws=ws)
+        K = max(5, min(args.steps, 50))
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+        torch.cuda.synchronize(dev)
+        for i in range(K):
+            moe.moe_forward_events(x, logits, W1, W3, W2, base.k, evs[i], out=out, ws=ws)
+        torch.cuda.synchronize(dev)
+        if moe.moe_get_device_status(ws) != 0:
+            raise RuntimeError("device status after sweep point")
+        step = statistics.median(evs[i][0].elapsed_time(evs[i][nst]) for i in range(K))
+        ffn = statistics.median(evs[i][4].elapsed_time(evs[i][6]) for i in range(K))
+        flops = acc.ffn_flops(T, base.H, base.F, base.k)
+        util = acc.util(base.k, base.E, peaks["hbm_gbs"] * 1e9, peaks["bf16_tflops"] * 1e12, T)
+        points.append({"tokens_per_expert": be, "T": T, "layer_ms": round(step, 5),
+                       "ffn_ms": round(ffn, 5), "ffn_tflops": round(flops / ffn / 1e9, 2),
+                       "ffn_frac_of_peak": round(flops / ffn / 1e9 / peaks["bf16_tflops"], 4),
+                       "util_model": round(util, 4)})
+    # least squares Te = k3 * b_e + k4 on the FFN time
+    xs = [p["tokens_per_expert"] for p in points]
+    ys = [p["ffn_ms"] * 1e3 for p in points]
+    n = len(xs)
+    mx, my = sum(xs) / n, sum(ys) / n
+    sxx = sum((a - mx) ** 2 for a in xs)
+    sxy = sum((a - mx) * (b - my) for a, b in zip(xs, ys))
+    k3 = sxy / sxx
+    k4 = my - k3 * mx
+    ss_res = sum((b - (k3 * a + k4)) ** 2 for a, b in zip(xs, ys))
+    ss_tot = sum((b - my) ** 2 for b in ys)
+    ridge = acc.ridge_tokens(peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+    return {"sweep": "tokens_per_expert", "shape": {"H": base.H, "F": base.F, "E": base.E,
+                                                    "k": base.k},
+            "peaks": {**peaks, "source": peak_src},
+            "ridge_tokens_per_expert": round(ridge * base.k / base.E, 1),
+            "fit_Te_us": {"k3_us_per_token": round(k3, 4), "k4_us": round(k4, 2),
+                          "r2": round(1 - ss_res / ss_tot, 5)},
+            "points": points}
+
+
 def main():
     args = parse()
+    if args.sweep:
+        print(json.dumps(bench_sweep(args)), flush=True)
+        return
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist

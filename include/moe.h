@@ -219,6 +219,17 @@ const char* moe_forward_stage_name(int i);
  */
 moe_status moe_get_device_status(const void* ws, void* stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): runs the bounded wait that
+ * every pipeline wait of the grouped GEMM uses on a barrier that nothing
+ * arrives on.  After `limit_ns` (1 ms .. 2 s, else MOE_ERR_INVALID_ARG) the
+ * wait gives up and MOE_ERR_TIMEOUT is written to the status word of `ws`,
+ * which moe_get_device_status then returns; the CUDA context stays usable.
+ * It lets a test check the timeout path without faulting or hanging a GPU.
+ */
+moe_status moe_diag_wait_timeout(void* ws, size_t ws_bytes, long long limit_ns,
+                                 void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* moe_status_string(moe_status s);
 

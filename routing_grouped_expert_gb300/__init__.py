@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     MoeError,
     load_library,
     moe_combine,
+    moe_diag_wait_timeout,
     moe_forward,
     moe_forward_events,
     moe_forward_stage_name,

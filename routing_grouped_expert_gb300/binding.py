@@ -36,6 +36,7 @@ SIGNATURES = {
     "moe_forward_stage_name": (ctypes.c_char_p, [_I]),
     "moe_get_device_status": (_I, [_VP, _VP]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_diag_wait_timeout": (_I, [_VP, _SZ, ctypes.c_longlong, _VP]),
 }
 
 
@@ -134,6 +135,12 @@ def moe_status_string(code: int) -> str:
 def moe_get_device_status(ws: Workspace) -> int:
     """Synchronises the current stream; returns the device status word."""
     return int(load_library().moe_get_device_status(ws.ptr, _stream()))
+
+
+def moe_diag_wait_timeout(ws: Workspace, limit_ns: int) -> None:
+    """Make a bounded device wait run out (see include/moe.h)."""
+    _check(load_library().moe_diag_wait_timeout(ws.ptr, ws.nbytes, limit_ns, _stream()),
+           "moe_diag_wait_timeout")
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None,

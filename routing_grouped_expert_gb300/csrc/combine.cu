@@ -27,15 +27,15 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
                __nv_bfloat16* __restrict__ out) {
   __shared__ int s_row[MOE_MAX_TOPK];
   __shared__ float s_w[MOE_MAX_TOPK];
-  const int t = blockIdx.y;
+  const int t = blockIdx.x;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = dest_of[(size_t)t * k + threadIdx.x];
     s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
   const int nv = H / 8;
-  for (int v = blockIdx.x * kCombineThreads + threadIdx.x; v < nv;
-       v += gridDim.x * kCombineThreads) {
+  for (int v = blockIdx.y * kCombineThreads + threadIdx.x; v < nv;
+       v += gridDim.y * kCombineThreads) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -63,7 +63,8 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int slices = (H / 8 + kCombineThreads - 1) / kCombineThreads;
-  combine_kernel<<<dim3(slices, T), kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k,
+  // tokens on the x dimension (up to 2^31 - 1), column slices on y
+  combine_kernel<<<dim3(T, slices), kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k,
                                                             out);
   return cudaGetLastError();
 }

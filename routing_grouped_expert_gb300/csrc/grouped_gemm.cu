@@ -9,11 +9,13 @@
 // ("Piper", §III-A, Table III).
 //
 // Tile = (expert e, token block b, feature tile m): the expert's rows are cut
-// into blocks of at most 128 rows, so each expert has at most one partial
-// block ("MegaFlux", §3.1).  The GEMM is computed transposed (D^T = W^T X^T):
-// the weight tile is the 128-row M operand, read MN-major straight from the
-// caller's [E, K, N] layout; the token block is the N operand (N = rows
-// rounded up to 16), so a skinny decode block costs no padded MMA work.
+// into ceil(rows / beta) blocks, as in "MegaFlux" §3.1 (blocks of at most
+// beta rows), here of equal size rather than full blocks plus one partial
+// one, so no block is a near-empty tail.  The GEMM is computed transposed
+// (D^T = W^T X^T): the weight tile is the 128-row M operand, read MN-major
+// straight from the caller's [E, K, N] layout; the token block is the N
+// operand (N = rows rounded up to 16), so a skinny decode block costs no
+// padded MMA work.
 //
 // Scheduling: every CTA is persistent (one per SM) and walks the flat tile
 // list round-robin.  Tiles are ordered expert-major, then in groups of up to
@@ -24,9 +26,10 @@
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2-5 = epilogue (TMEM -> registers -> global).  Shared
-// memory holds a ring of operand stages; TMEM holds two accumulator buffers
-// so the epilogue of one tile overlaps the MMAs of the next.  Every wait is
-// bounded; a wait that runs out sets MOE_ERR_TIMEOUT and all roles leave.
+// memory holds a ring of operand stages; where TMEM has room for two
+// accumulator buffers the epilogue of one tile overlaps the MMAs of the
+// next.  Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT
+// and all roles leave.
 #include <cuda.h>
 
 #include "moe_common.cuh"
@@ -77,7 +80,7 @@ struct Bars {
 static_assert(sizeof(Bars) <= 256, "barrier block too large");
 
 struct Item {
-  int e, row0, nrows, mt;
+  int e, row0, nrows, mt, nb;   // nb: token blocks of this expert
 };
 
 // Flat tile index -> (expert, first row, rows, feature tile).
@@ -95,11 +98,20 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   const int r = local - g * gspan;
   const int mt = r / gsize;
   const int b = g * kGroupBlocks + (r - mt * gsize);
+  // The expert's rows are cut into nb blocks of equal size (a multiple of
+  // 16 rows, at most kBN): a block count above one then never leaves a
+  // near-empty tail block that would stream the whole weight tile for a
+  // handful of rows.  Since size <= kBN and nb = ceil(rows / kBN), the last
+  // block is never empty.
+  const int beg = offsets[e];
+  const int cnt = offsets[e + 1] - beg;
+  const int bsz = min(kBN, ((cnt + nb - 1) / nb + 15) & ~15);
   Item it;
   it.e = e;
   it.mt = mt;
-  it.row0 = offsets[e] + b * kBN;
-  it.nrows = min(kBN, offsets[e + 1] - it.row0);
+  it.row0 = beg + b * bsz;
+  it.nrows = min(bsz, cnt - b * bsz);
+  it.nb = nb;
   return it;
 }
 
@@ -152,11 +164,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      // Weights: with 128-row blocks (decode-like layers) each weight tile has
-      // one consumer and is streamed past L2; with 256-row blocks the sibling
-      // blocks of an expert read the same tile moments later, so it stays.
-      const uint64_t pol_w =
-          (kBN == kBlockRowsLarge) ? policy_evict_normal() : policy_evict_first();
+      // Weights: a tile read by a single token block is streamed past L2
+      // (evict-first); when an expert has several blocks, its sibling blocks
+      // read the same tile moments later, so it is kept (evict-normal).
+      const uint64_t pol_once = policy_evict_first();
+      const uint64_t pol_shared = policy_evict_normal();
       const uint64_t pol_x = policy_evict_last();    // token rows: reused
       int stage = 0, issued = 0;
       uint32_t phase = 0;
@@ -166,6 +178,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
         const uint32_t bytes = kNumA * kABytes + nbox * kBBoxBytes;
         const int f0 = it.mt * C::kFeatPerItem;
+        const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -383,15 +396,19 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   return cudaGetLastError();
 }
 
-// Tile configuration of a layer: decode-like layers (at most 128 routed rows
-// per expert on average) keep 128-row blocks and double-buffered
+// Tile configuration of a layer: decode-like layers (few routed rows per
+// expert) keep 128-row blocks and double-buffered
 // accumulators so a tile's epilogue overlaps the next tile's weight stream;
 // larger layers use 256-row blocks and two 128-row weight tiles per CTA
 // tile, which halves the operand bytes each SM pulls from L2 per FLOP.
 enum class FfnMode { kSmall, kLarge };
 
-FfnMode ffn_mode(int P, int E) { return (P <= kBlockRows * (long long)E) ? FfnMode::kSmall
-                                                                          : FfnMode::kLarge; }
+// Small mode while the mean is at most 80 rows per expert: with uniform
+// routing the largest expert then stays within one 128-row block.
+constexpr int kSmallModeMeanRows = 80;
+FfnMode ffn_mode(int P, int E) {
+  return ((long long)P <= (long long)kSmallModeMeanRows * E) ? FfnMode::kSmall : FfnMode::kLarge;
+}
 
 // FC2 pairs two W2 tiles when H allows it and K is long enough that the
 // single-buffered epilogue is a small share of a tile.

@@ -24,6 +24,8 @@ CASES = {  # name: (T, H, F, E, k, skew_alpha)
     "k_equals_E": (50, 128, 256, 3, 3, 0.0),
     # > 128 rows per expert: 256-row blocks; F >= 4096 pairs two W2 tiles in FC2
     "large_blocks_paired_fc2": (600, 512, 4096, 2, 2, 0.0),
+    # more tokens than a grid's y dimension holds (65535)
+    "many_tokens": (70000, 128, 128, 4, 1, 0.0),
 }
 
 
