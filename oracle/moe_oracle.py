@@ -35,6 +35,14 @@ Sources for each step:
   weighted top-k sum back to token order:
       "MegaFlux", §2.1; "MegaScale-Infer", §3.2 step (4)-(5).
 
+Either side of the routed path ("forward_gated"):
+  router projection: the gating network that decides each token's experts
+      ("MegaScale-Infer", §3.2 Big-Picture Architecture, item 2; "Piper",
+      §II-A: a learned gating function), read as logits = x @ W_g;
+  shared expert: an always-active expert next to the routed ones ("Piper",
+      Table I, e.g. "8R + 1S" = 8 routed + 1 shared per token), read as a
+      SwiGLU expert applied to every token and added with weight one.
+
 Readings where the pages are silent (each is listed in the design notes):
   * experts are ranked on the raw fp32 logits; a larger value wins, equal
     values (including -0.0 == +0.0) go to the lower expert index;
@@ -44,7 +52,9 @@ Readings where the pages are silent (each is listed in the design notes):
   * W1 is the gate (silu applied), W3 the up projection, W2 the down
     projection;
   * non-finite logits are rejected;
-  * no capacity limit: every routed assignment is computed (dropless).
+  * no capacity limit: every routed assignment is computed (dropless);
+  * the router has no bias; its logits are the layer's fp32 router output,
+    so forward_gated rounds the fp64 product to fp32 before ranking.
 
 Floating point: bf16 and fp32 inputs convert exactly to fp64; all sums are
 fp64; no intermediate is rounded.  Matrix products use a library matmul
@@ -232,3 +242,28 @@ def forward_direct(x, logits, W1, W3, W2, k: int, tokens=None) -> np.ndarray:
     for j in range(k):
         out += wt[:, j:j + 1] * Y[:, j]
     return out
+
+
+# --------------------------------------------------------------------------
+# Either side of the routed path: router projection and a shared expert
+# --------------------------------------------------------------------------
+def router_logits(x, Wg) -> np.ndarray:
+    """logits[t, e] = sum_h x[t, h] * Wg[h, e], fp64 (Wg is [H, E])."""
+    return _mm(_f64(x), _f64(Wg))
+
+
+def forward_gated(x, Wg, W1, W3, W2, k: int, shared=None, logits=None):
+    """The layer from hidden states.
+
+    logits = x @ Wg rounded to fp32 (or the fp32 `logits` given, so a test can
+    rank on another implementation's router output), the routed experts as in
+    forward_perm, and -- when `shared` = (Ws1, Ws3, Ws2) -- the shared expert
+    FFN_s(x[t]) added to every token's output with weight one."""
+    l = (np.asarray(router_logits(x, Wg), dtype=np.float32) if logits is None
+         else np.asarray(logits, dtype=np.float32))
+    r = forward_perm(x, l, W1, W3, W2, k)
+    r["logits"] = l
+    if shared is not None:
+        r["shared"] = expert_ffn(x, *shared)
+        r["out"] = r["out"] + r["shared"]
+    return r

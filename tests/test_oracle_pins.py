@@ -230,6 +230,46 @@ def test_empty_batch():
     assert r["counts"].sum() == 0 and np.all(r["offsets"] == 0)
 
 
+# ------------------------------------------------ router and shared expert
+def check_router_brute(router=None, seed=16):
+    router = router or O.router_logits
+    rng = np.random.default_rng(seed)
+    T, H, E = 4, 5, 3                       # non-square: a transpose cannot pass
+    x, Wg = rng.standard_normal((T, H)), rng.standard_normal((H, E))
+    want = [[sum(float(x[t][h]) * float(Wg[h][e]) for h in range(H)) for e in range(E)]
+            for t in range(T)]
+    np.testing.assert_allclose(router(x, Wg), want, rtol=1e-12, atol=1e-12)
+
+
+def test_router_logits_brute_force():
+    check_router_brute()
+
+
+def test_gated_layer_routes_on_fp32_router_output():
+    x, _, W1, W3, W2 = rand_layer(40, 32, 48, 6, 2, seed=17)
+    Wg = torch.randn(32, 6, generator=torch.Generator().manual_seed(18)).to(torch.bfloat16)
+    r = O.forward_gated(x, Wg, W1, W3, W2, 2)
+    l32 = (x.double() @ Wg.double()).numpy().astype(np.float32)
+    np.testing.assert_array_equal(r["logits"], l32)
+    np.testing.assert_allclose(r["out"], O.forward_perm(x, l32, W1, W3, W2, 2)["out"],
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_shared_expert_adds_the_dense_ffn():
+    # E = 1, k = 1 and a shared expert equal to the routed one: out = 2 * FFN(x)
+    x, _, W1, W3, W2 = rand_layer(30, 32, 64, 1, 1, seed=19)
+    Wg = torch.randn(32, 1, generator=torch.Generator().manual_seed(20)).to(torch.bfloat16)
+    r = O.forward_gated(x, Wg, W1, W3, W2, 1, shared=(W1[0], W3[0], W2[0]))
+    xd = x.double()
+    dense = (torch.nn.functional.silu(xd @ W1[0].double()) * (xd @ W3[0].double())) \
+        @ W2[0].double()
+    np.testing.assert_allclose(r["out"], 2 * dense.numpy(), rtol=1e-12, atol=1e-12)
+    # a zero shared expert changes nothing
+    z = torch.zeros_like(W1[0]), torch.zeros_like(W3[0]), torch.zeros_like(W2[0])
+    r0 = O.forward_gated(x, Wg, W1, W3, W2, 1, shared=z)
+    np.testing.assert_allclose(r0["out"], dense.numpy(), rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------- the pages' own numbers
 def test_util_formula_a100_example():
     g = json.load(open(os.path.join(GOLDEN, "util_a100_example.json")))
@@ -318,3 +358,7 @@ def test_pins_catch_planted_mistakes():
         return counts, offsets, src, dest
     with pytest.raises(AssertionError):
         check_permute(permute_rev)
+
+    # 7. router computed with the transposed product
+    with pytest.raises((AssertionError, ValueError, RuntimeError)):
+        check_router_brute(lambda x, Wg: O.router_logits(x, np.asarray(Wg).T))
