@@ -53,6 +53,11 @@ def parse():
                     help="T,H,F,E,k: a uniform-routing workload of these sizes instead")
     ap.add_argument("--sweep", action="store_true",
                     help="tokens-per-expert sweep of the workload's shape (own JSON line)")
+    ap.add_argument("--gated", action="store_true",
+                    help="time the layer from hidden states (router projection + routed "
+                         "experts + --shared-f shared expert) instead (own JSON line)")
+    ap.add_argument("--shared-f", type=int, default=0,
+                    help="FFN width of the shared expert for --gated (0 = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -513,8 +518,62 @@ def bench_sweep(args):
             "points": points}
 
 
+# ----------------------------------------------- layer from hidden states
+def bench_gated(args):
+    """moe_forward_gated: router projection x @ Wg, the routed layer, and an
+    optional shared expert of width --shared-f added to every token."""
+    import routing_grouped_expert_gb300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[args.workload]
+    d = I.make_inputs(wl, dev)
+    g = torch.Generator(device=dev).manual_seed(6)
+    Wg = (torch.randn(wl.H, wl.E, generator=g, device=dev) / math.sqrt(wl.H)).to(torch.bfloat16)
+    Fs = args.shared_f
+    shared = None
+    if Fs:
+        shared = tuple((torch.randn(r, c, generator=g, device=dev) / math.sqrt(r)).to(
+            torch.bfloat16) for r, c in ((wl.H, Fs), (wl.H, Fs), (Fs, wl.H)))
+    ws = moe.Workspace(dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    run = lambda: moe.moe_forward_gated(d["x"], Wg, d["W1"], d["W3"], d["W2"], wl.k,  # noqa
+                                        shared=shared, out=out, ws=ws)
+    for _ in range(args.warmup):
+        run()
+    if moe.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks, peak_src = load_peaks()
+    idx = moe.moe_route_topk(moe.moe_router_logits(d["x"], Wg), wl.k)[0]
+    touched = int((moe.moe_permute(idx, wl.E)[0] > 0).sum())
+    flops = acc.ffn_flops(wl.T, wl.H, wl.F, wl.k) + 2 * wl.T * wl.H * wl.E \
+        + 2 * wl.T * 3 * wl.H * Fs
+    nbytes = acc.layer_bytes(wl.T, wl.H, wl.F, wl.E, wl.k, touched) + wl.H * wl.E * 2 \
+        + 3 * wl.H * Fs * 2
+    t_roof, bound = acc.roofline_seconds(flops, nbytes, peaks["bf16_tflops"] * 1e12,
+                                         peaks["hbm_gbs"] * 1e9)
+    return {"metric": METRIC, "mode": "gated", "value": round(wl.T / (ms / 1e3), 1),
+            "unit": UNIT, "ms_per_step": round(ms, 5), "steps": args.steps,
+            "config": wl_config(wl, {"router": f"x @ Wg [{wl.H}, {wl.E}] bf16 -> fp32",
+                                     "shared_expert_F": Fs, "touched_experts": touched}),
+            "layer_roofline": {"flops": flops, "bytes": nbytes, "t_roof_ms": round(t_roof * 1e3, 4),
+                               "bound": bound, "frac": round(t_roof / (ms / 1e3), 4),
+                               "tflops": round(flops / (ms / 1e3) / 1e12, 2),
+                               "peak_source": peak_src}}
+
+
 def main():
     args = parse()
+    if args.gated:
+        print(json.dumps(bench_gated(args)), flush=True)
+        return
     if args.sweep:
         print(json.dumps(bench_sweep(args)), flush=True)
         return

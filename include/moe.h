@@ -196,6 +196,40 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host,
                             void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The steps either side of the routed path.
+ *
+ * Router projection ("MegaScale-Infer" §3.2, item 2: the gating network
+ * decides each token's experts; "Piper" §II-A: a learned gating function):
+ *   logits[T, E] fp32 = x[T, H] bf16 @ Wg[H, E] bf16, fp32 accumulation,
+ *   no bias.  E < 64: any E; E >= 64: E a multiple of 8.  H a multiple of
+ *   128.  ws: at least 512 + 4 * (ceil(T/128) + 2) bytes (256-byte aligned);
+ *   moe_workspace_size_gated covers it.
+ */
+moe_status moe_router_logits(const void* x, const void* Wg, int T, int H, int E,
+                             float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for moe_forward_gated (Fs = 0 when there is no shared
+ * expert); 0 on bad sizes. */
+size_t moe_workspace_size_gated(int T, int H, int F, int Fs, int E, int k);
+
+/*
+ * The layer from hidden states: router projection, then moe_forward's four
+ * steps, plus an optional always-active shared expert ("Piper", Table I:
+ * "R + S" = routed + shared experts per token) applied to every token and
+ * added with weight one after the routed slots:
+ *   out[t] = sum_j w[t,j] FFN_{e[t,j]}(x[t]) + FFN_s(x[t]).
+ *   Wg [H, E] bf16; W1/W3 [E, H, F], W2 [E, F, H] bf16;
+ *   Ws1/Ws3 [H, Fs], Ws2 [Fs, H] bf16, all three NULL for no shared expert;
+ *   Fs a multiple of 128 when present.  Routing is decided on the fp32
+ *   router logits.  ws: moe_workspace_size_gated bytes.
+ */
+moe_status moe_forward_gated(const void* x, const void* Wg,
+                             const void* W1, const void* W3, const void* W2,
+                             const void* Ws1, const void* Ws3, const void* Ws2,
+                             int T, int H, int F, int Fs, int E, int k, void* out,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_forward with timing marks: records events[0] on `stream` before the
  * first kernel and events[i] after stage i, for the MOE_FORWARD_STAGES
  * stages route, scan, scatter, gather, fc1, fc2, combine (in that order).

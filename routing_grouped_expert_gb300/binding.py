@@ -37,6 +37,10 @@ SIGNATURES = {
     "moe_get_device_status": (_I, [_VP, _VP]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_diag_wait_timeout": (_I, [_VP, _SZ, ctypes.c_longlong, _VP]),
+    "moe_router_logits": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_workspace_size_gated": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_gated": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                               _VP, _VP, _SZ, _VP]),
 }
 
 
@@ -274,3 +278,50 @@ def moe_forward_host(x_host, logits_host, W1, W3, W2, k: int, out_host=None,
                                            T, H, F, E, k, _p(out_host), ws.ptr, ws.nbytes,
                                            _stream()), "moe_forward_host")
     return out_host
+
+
+# ------------------------------------------ either side of the routed path
+def moe_workspace_size_gated(T: int, H: int, F: int, Fs: int, E: int, k: int) -> int:
+    return int(load_library().moe_workspace_size_gated(T, H, F, Fs, E, k))
+
+
+def moe_router_logits(x, Wg, logits=None, ws: Workspace | None = None):
+    """logits [T, E] fp32 = x [T, H] @ Wg [H, E] (bf16 in)."""
+    T, H = x.shape
+    E = Wg.shape[1]
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(Wg, torch.bfloat16, (H, E), "Wg")
+    logits = torch.empty(T, E, dtype=torch.float32, device=x.device) if logits is None \
+        else logits
+    _need(logits, torch.float32, (T, E), "logits")
+    ws = _ws(ws, 1024 + 4 * (T // 128 + 4))
+    _check(load_library().moe_router_logits(_p(x), _p(Wg), T, H, E, _p(logits), ws.ptr,
+                                            ws.nbytes, _stream()), "moe_router_logits")
+    return logits
+
+
+def moe_forward_gated(x, Wg, W1, W3, W2, k: int, shared=None, out=None,
+                      ws: Workspace | None = None):
+    """Router projection + routed experts (+ `shared` = (Ws1, Ws3, Ws2))."""
+    T, H = x.shape
+    E, _, F = W1.shape
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(Wg, torch.bfloat16, (H, E), "Wg")
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    Fs = 0
+    if shared is not None:
+        Ws1, Ws3, Ws2 = shared
+        Fs = Ws1.shape[1]
+        _need(Ws1, torch.bfloat16, (H, Fs), "Ws1")
+        _need(Ws3, torch.bfloat16, (H, Fs), "Ws3")
+        _need(Ws2, torch.bfloat16, (Fs, H), "Ws2")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out, torch.bfloat16, (T, H), "out")
+    ws = _ws(ws, moe_workspace_size_gated(T, H, F, Fs, E, k))
+    sp = (None, None, None) if shared is None else tuple(_p(t) for t in shared)
+    _check(load_library().moe_forward_gated(_p(x), _p(Wg), _p(W1), _p(W3), _p(W2), *sp, T, H,
+                                            F, Fs, E, k, _p(out), ws.ptr, ws.nbytes, _stream()),
+           "moe_forward_gated")
+    return out

@@ -24,7 +24,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const int4& v, float (&f)[8]) {
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __restrict__ dest_of,
                const float* __restrict__ topk_w, int H, int k,
-               __nv_bfloat16* __restrict__ out) {
+               __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ y_shared) {
   __shared__ int s_row[MOE_MAX_TOPK];
   __shared__ float s_w[MOE_MAX_TOPK];
   const int t = blockIdx.x;
@@ -48,6 +48,13 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
     }
+    if (y_shared != nullptr) {   // always-active expert, weight one, after the slots
+      const int4 raw = __ldg(reinterpret_cast<const int4*>(y_shared + (size_t)t * H) + v);
+      float f[8];
+      bf16x8_to_f32(raw, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
     int4 o;
     __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
@@ -60,12 +67,12 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
 
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
-                           cudaStream_t s) {
+                           cudaStream_t s, const __nv_bfloat16* y_shared) {
   if (T == 0) return cudaSuccess;
   const int slices = (H / 8 + kCombineThreads - 1) / kCombineThreads;
   // tokens on the x dimension (up to 2^31 - 1), column slices on y
   combine_kernel<<<dim3(T, slices), kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k,
-                                                            out);
+                                                            out, y_shared);
   return cudaGetLastError();
 }
 

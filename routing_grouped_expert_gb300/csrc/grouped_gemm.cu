@@ -52,8 +52,9 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 // kNumA weight tiles of 128 rows share each token block:
 //   FC1 (kGLU): gate and up tiles of the same 128 features;
 //   FC2 with kNumA = 2: two adjacent 128-feature tiles of W2.
-// kBN = token rows per block (beta), kAccBufs = TMEM accumulator buffers.
-template <int kNumA, bool kGLU, int kBN, int kAccBufs>
+// kBN = token rows per block (beta), kAccBufs = TMEM accumulator buffers,
+// kOutF32 = fp32 output (router logits) instead of bf16.
+template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32 = false>
 struct Cfg {
   static constexpr int kBBytes = kBN * BK * 2;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
@@ -66,6 +67,7 @@ struct Cfg {
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
+  static_assert(!kOutF32 || (kNumA == 1 && !kGLU), "fp32 output: single plain tile");
 };
 
 struct Bars {
@@ -115,7 +117,7 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   return it;
 }
 
-template <int kNumA, bool kGLU, int kBN, int kAccBufs>
+template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -123,8 +125,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ block_off,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
-                    __nv_bfloat16* __restrict__ out, int ld_out, int* __restrict__ status) {
-  using C = Cfg<kNumA, kGLU, kBN, kAccBufs>;
+                    void* __restrict__ out_ptr, int ld_out, int m_valid,
+                    int* __restrict__ status) {
+  using C = Cfg<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -290,7 +293,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       tc_fence_after();
       const int feat = it.mt * C::kFeatPerItem + q * 32 + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      __nv_bfloat16* col = out + (size_t)it.row0 * ld_out + feat;
+      if constexpr (kOutF32) {
+        // fp32 output; rows of a partial weight tile (feature >= m_valid) are
+        // zero padding and are not stored.
+        float* col = static_cast<float*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
+        const bool store = feat < m_valid;
+        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+          uint32_t g[16];
+          tmem_ld_32x32b_x16(tb + c0, g);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (store && c0 + c < it.nrows) col[(size_t)(c0 + c) * ld_out] = __uint_as_float(g[c]);
+        }
+      } else {
+      __nv_bfloat16* col =
+          static_cast<__nv_bfloat16*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
       for (int c0 = 0; c0 < it.nrows; c0 += 16) {
         uint32_t g[16];
         tmem_ld_32x32b_x16(tb + c0, g);
@@ -324,6 +342,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if (c0 + c < it.nrows)
               col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(__uint_as_float(g[c]));
         }
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -377,22 +396,25 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kNumA, bool kGLU, int kBN, int kAccBufs>
+template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32 = false>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
-                        int K, long long nb_max, __nv_bfloat16* out, int ld_out, int* status,
+                        int K, long long nb_max, void* out, int ld_out, int* status,
                         cudaStream_t s) {
-  using C = Cfg<kNumA, kGLU, kBN, kAccBufs>;
-  auto kern = grouped_gemm_kernel<kNumA, kGLU, kBN, kAccBufs>;
+  using C = Cfg<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
+  auto kern = grouped_gemm_kernel<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const int n_mt = M_total / C::kFeatPerItem;
+  // a partial last feature tile (router with E not a multiple of 128) is
+  // zero-filled by the TMA and not stored
+  const int n_mt = (M_total + C::kFeatPerItem - 1) / C::kFeatPerItem;
   const long long items = nb_max * n_mt;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, offsets, block_off, num_blocks,
-                                             block_expert, n_mt, K, out, ld_out, status);
+                                             block_expert, n_mt, K, out, ld_out, M_total,
+                                             status);
   return cudaGetLastError();
 }
 
@@ -468,6 +490,31 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                                      H, status, s);
   return launch_gemm<1, false, kBlockRowsLarge, 2>(mW2, mW2, mH, offsets, block_off, num_blocks,
                                                    block_expert, H, F, nb_max, y, H, status, s);
+}
+
+cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T, int H,
+                               int E, const int32_t* offsets, const int32_t* block_off,
+                               const int32_t* num_blocks, const int32_t* block_expert,
+                               float* logits, int* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  // logits^T = Wg^T x^T: one "expert" whose weight matrix is Wg [H, E]
+  CUtensorMap mG, mX;
+  const cuuint64_t dG[3] = {(cuuint64_t)E, (cuuint64_t)H, 1};
+  const cuuint64_t sG[2] = {(cuuint64_t)E * 2, (cuuint64_t)H * E * 2};
+  const cuuint32_t boxW[3] = {64, (cuuint32_t)BK, 1};
+  const cuuint64_t dX[2] = {(cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t sX[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t boxRows[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
+  if (!make_map(&mG, Wg, 3, dG, sG, boxW) || !make_map(&mX, x, 2, dX, sX, boxRows))
+    return cudaErrorInvalidValue;
+  if (ffn_mode(T, 1) == FfnMode::kSmall)
+    return launch_gemm<1, false, kBlockRows, 2, true>(mG, mG, mX, offsets, block_off, num_blocks,
+                                                      block_expert, E, H,
+                                                      max_blocks(T, 1, kBlockRows), logits, E,
+                                                      status, s);
+  return launch_gemm<1, false, kBlockRowsLarge, 2, true>(
+      mG, mG, mX, offsets, block_off, num_blocks, block_expert, E, H,
+      max_blocks(T, 1, kBlockRowsLarge), logits, E, status, s);
 }
 
 }  // namespace moe

@@ -73,12 +73,26 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 const char* const kStageNames[MOE_FORWARD_STAGES] = {"route", "scan", "scatter", "gather",
                                                      "fc1", "fc2", "combine"};
 
+// An always-active expert run over every token in order.
+struct SharedExpert {
+  const void* W1;
+  const void* W3;
+  const void* W2;
+  int Fs;
+  SingleExpertPlan plan;
+  __nv_bfloat16* h;   // [T, Fs]
+  __nv_bfloat16* y;   // [T, H]
+};
+
 // The launch sequence of the whole layer on device buffers.  With `ev`
-// non-null, ev[0] is recorded first and ev[i] after stage i.
+// non-null, ev[0] is recorded first and ev[i] after stage i.  With
+// `clear` false the caller has already zeroed the status word and the chunk
+// table.  With `sh` the shared expert's output is added in the combine.
 moe_status forward_device(const void* x, const float* logits, const void* W1, const void* W3,
                           const void* W2, int T, int H, int F, int E, int k, void* out,
                           void* ws, const WsLayout& L, cudaStream_t s,
-                          const cudaEvent_t* ev = nullptr) {
+                          const cudaEvent_t* ev = nullptr, bool clear = true,
+                          const SharedExpert* sh = nullptr) {
   const int P = T * k;
   const int C = num_chunks(T, k);
   int* status = ws_ptr<int>(ws, L.status);
@@ -98,8 +112,9 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
 
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
   // status word and the chunk histogram table (adjacent) start at zero
-  MOE_TRY(cudaMemsetAsync(status, 0, L.chunk_base - L.status + (size_t)C * E * sizeof(int32_t),
-                          s));
+  if (clear)
+    MOE_TRY(cudaMemsetAsync(status, 0,
+                            L.chunk_base - L.status + (size_t)C * E * sizeof(int32_t), s));
   MOE_TRY(mark(0));
   MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
   MOE_TRY(mark(1));
@@ -115,8 +130,16 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
                              ev ? ev[5] : nullptr));
+  if (sh != nullptr)
+    MOE_TRY(launch_grouped_ffn(static_cast<const __nv_bfloat16*>(x), sh->plan.offsets,
+                               sh->plan.block_off, sh->plan.num_blocks, sh->plan.block_expert,
+                               static_cast<const __nv_bfloat16*>(sh->W1),
+                               static_cast<const __nv_bfloat16*>(sh->W3),
+                               static_cast<const __nv_bfloat16*>(sh->W2), T, H, sh->Fs, 1, sh->h,
+                               sh->y, status, s));
   MOE_TRY(mark(6));
-  MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s));
+  MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
+                         sh ? sh->y : nullptr));
   MOE_TRY(mark(7));
   return MOE_OK;
 }
@@ -280,6 +303,80 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
   if (st != MOE_OK) return st;
   MOE_TRY(cudaMemcpyAsync(out_host, dout, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
+}
+
+size_t moe_workspace_size_gated(int T, int H, int F, int Fs, int E, int k) {
+  if (!ok_sizes(T, H, F, E, k) || Fs < 0 || (Fs > 0 && (Fs % kTileM != 0)) ||
+      (E >= 64 && E % 8 != 0))
+    return 0;
+  return gated_layout(T, H, F, Fs, E, k).total;
+}
+
+namespace {
+// Router-only workspace: status word, then the single-expert plan.
+constexpr size_t kRouterPlanOffset = 256;
+size_t router_ws_bytes(int T) { return kRouterPlanOffset + 64 + 4 * ((size_t)max_blocks(T, 1) + 1); }
+SingleExpertPlan router_plan(void* ws) {
+  int32_t* p = ws_ptr<int32_t>(ws, kRouterPlanOffset);
+  return SingleExpertPlan{p, p + 2, p + 4, p + 16};
+}
+bool ok_router_sizes(int T, int H, int E) {
+  return T >= 0 && H >= kTileM && H % kTileM == 0 && E >= 1 && E <= MOE_MAX_EXPERTS &&
+         (E < 64 || E % 8 == 0) && (long long)T * E < (1LL << 40);
+}
+}  // namespace
+
+moe_status moe_router_logits(const void* x, const void* Wg, int T, int H, int E, float* logits,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_router_sizes(T, H, E)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(Wg) || !ok_ptr(logits)) return MOE_ERR_INVALID_ARG;
+  if (check_ws(ws, ws_bytes, router_ws_bytes(T)) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(ws);
+  const SingleExpertPlan plan = router_plan(ws);
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  if (E >= 64) MOE_TRY(launch_single_expert_plan(T, ffn_block_rows(T, 1, H, E), plan, s));
+  MOE_TRY(launch_router(static_cast<const __nv_bfloat16*>(x),
+                        static_cast<const __nv_bfloat16*>(Wg), T, H, E, plan, logits, status, s));
+  return MOE_OK;
+}
+
+moe_status moe_forward_gated(const void* x, const void* Wg, const void* W1, const void* W3,
+                             const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                             int T, int H, int F, int Fs, int E, int k, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  const bool shared = Ws1 != nullptr || Ws3 != nullptr || Ws2 != nullptr;
+  if (!ok_sizes(T, H, F, E, k) || !ok_router_sizes(T, H, E)) return MOE_ERR_INVALID_ARG;
+  if (shared && (Fs < kTileM || Fs % kTileM != 0)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(Wg) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) || !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  if (shared && (!ok_ptr(Ws1) || !ok_ptr(Ws3) || !ok_ptr(Ws2))) return MOE_ERR_INVALID_ARG;
+  const GatedLayout G = gated_layout(T, H, F, shared ? Fs : 0, E, k);
+  if (check_ws(ws, ws_bytes, G.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout& L = G.base;
+  int* status = ws_ptr<int>(ws, L.status);
+  float* logits = ws_ptr<float>(ws, G.logits);
+  const SingleExpertPlan plan{ws_ptr<int32_t>(ws, G.s_offsets), ws_ptr<int32_t>(ws, G.s_block_off),
+                              ws_ptr<int32_t>(ws, G.s_num_blocks),
+                              ws_ptr<int32_t>(ws, G.s_block_expert)};
+  // status word and chunk table first: the router may report into it
+  MOE_TRY(cudaMemsetAsync(status, 0,
+                          L.chunk_base - L.status +
+                              (size_t)num_chunks(T, k) * E * sizeof(int32_t), s));
+  // the single-expert plan serves the tensor-core router and the shared expert
+  if (E >= 64 || shared)
+    MOE_TRY(launch_single_expert_plan(T, ffn_block_rows(T, 1, H, E), plan, s));
+  MOE_TRY(launch_router(static_cast<const __nv_bfloat16*>(x),
+                        static_cast<const __nv_bfloat16*>(Wg), T, H, E, plan, logits, status, s));
+  SharedExpert sh{Ws1, Ws3, Ws2, Fs, plan, ws_ptr<__nv_bfloat16>(ws, G.s_h),
+                  ws_ptr<__nv_bfloat16>(ws, G.s_y)};
+  return forward_device(x, logits, W1, W3, W2, T, H, F, E, k, out, ws, L, s, nullptr,
+                        /*clear=*/false, shared ? &sh : nullptr);
 }
 
 moe_status moe_get_device_status(const void* ws, void* stream) {

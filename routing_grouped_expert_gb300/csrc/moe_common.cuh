@@ -71,6 +71,20 @@ struct WsLayout {
   size_t total;
 };
 
+// Workspace of the layer from hidden states (router projection + routed
+// experts + optional shared expert): the routed layout, then these regions.
+struct GatedLayout {
+  WsLayout base;
+  size_t logits;        // f32[T*E]
+  size_t s_offsets;     // int32[2]
+  size_t s_block_off;   // int32[2]
+  size_t s_num_blocks;  // int32[1]
+  size_t s_block_expert;// int32[max_blocks(T, 1)]
+  size_t s_h;           // bf16[T*Fs]
+  size_t s_y;           // bf16[T*H]
+  size_t total;
+};
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
@@ -101,6 +115,22 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   return L;
 }
 
+inline GatedLayout gated_layout(int T, int H, int F, int Fs, int E, int k) {
+  GatedLayout G{};
+  G.base = ws_layout(T, H, F, E, k);
+  size_t o = G.base.total;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
+  G.logits = take((size_t)T * E * 4);
+  G.s_offsets = take(2 * 4);
+  G.s_block_off = take(2 * 4);
+  G.s_num_blocks = take(4);
+  G.s_block_expert = take((size_t)max_blocks(T, 1) * 4 + 4);
+  G.s_h = take((size_t)T * (Fs > 0 ? Fs : 0) * 2);
+  G.s_y = take((size_t)T * H * 2);
+  G.total = o;
+  return G;
+}
+
 template <typename Tp>
 inline Tp* ws_ptr(void* ws, size_t off) { return reinterpret_cast<Tp*>((char*)ws + off); }
 
@@ -129,9 +159,30 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
                                cudaStream_t s, cudaEvent_t after_fc1 = nullptr);
+// out[t] = sum_j w[t,j] y_sorted[dest_of[t*k+j]] (+ y_shared[t] when given)
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
-                           cudaStream_t s);
+                           cudaStream_t s, const __nv_bfloat16* y_shared = nullptr);
+
+// Block plan of one expert that takes every token in order (router GEMM,
+// shared expert): offsets = {0, T}.
+struct SingleExpertPlan {
+  int32_t* offsets;       // [2]
+  int32_t* block_off;     // [2]
+  int32_t* num_blocks;    // [1]
+  int32_t* block_expert;  // [max_blocks(T, 1)]
+};
+cudaError_t launch_single_expert_plan(int T, int beta, const SingleExpertPlan& plan,
+                                      cudaStream_t s);
+cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T, int H,
+                               int E, const int32_t* offsets, const int32_t* block_off,
+                               const int32_t* num_blocks, const int32_t* block_expert,
+                               float* logits, int* status, cudaStream_t s);
+// logits[T, E] fp32 = x[T, H] W_g[H, E]; E >= 64 on the tensor cores (the
+// plan must then be built with ffn_block_rows(T, 1, .., ..)).
+cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T, int H, int E,
+                          const SingleExpertPlan& plan, float* logits, int* status,
+                          cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
