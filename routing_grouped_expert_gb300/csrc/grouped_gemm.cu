@@ -46,7 +46,7 @@ constexpr int kAHalfBytes = 64 * BK * 2;          // one 64-feature TMA box: 8 K
 constexpr int kABytes = BM * BK * 2;              // 16 KB per weight tile per stage
 constexpr int kBBoxBytes = kRowBox * BK * 2;      // 32 token rows: 4 KB
 constexpr int kThreads = 192;
-constexpr int kSmemBudget = 196608;               // operand ring: 192 KB
+constexpr int kSmemBudget = 204800;               // operand ring: 200 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 // kNumA weight tiles of 128 rows share each token block:
@@ -64,7 +64,7 @@ struct Cfg {
   static constexpr int kFeatPerItem = kGLU ? BM : kNumA * BM;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
-  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
   static_assert(!kOutF32 || (kNumA == 1 && !kGLU), "fp32 output: single plain tile");
@@ -418,20 +418,6 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   return cudaGetLastError();
 }
 
-// Tile configuration of a layer: decode-like layers (few routed rows per
-// expert) keep 128-row blocks and double-buffered
-// accumulators so a tile's epilogue overlaps the next tile's weight stream;
-// larger layers use 256-row blocks and two 128-row weight tiles per CTA
-// tile, which halves the operand bytes each SM pulls from L2 per FLOP.
-enum class FfnMode { kSmall, kLarge };
-
-// Small mode while the mean is at most 80 rows per expert: with uniform
-// routing the largest expert then stays within one 128-row block.
-constexpr int kSmallModeMeanRows = 80;
-FfnMode ffn_mode(int P, int E) {
-  return ((long long)P <= (long long)kSmallModeMeanRows * E) ? FfnMode::kSmall : FfnMode::kLarge;
-}
-
 // FC2 pairs two W2 tiles when H allows it and K is long enough that the
 // single-buffered epilogue is a small share of a tile.
 #ifndef MOE_FC2_PAIR_MIN_F
@@ -444,7 +430,11 @@ bool fc2_paired(int H, int F) { return H % (2 * BM) == 0 && F >= MOE_FC2_PAIR_MI
 int ffn_block_rows(int P, int E, int H, int F) {
   (void)H;
   (void)F;
-  return ffn_mode(P, E) == FfnMode::kSmall ? kBlockRows : kBlockRowsLarge;
+  switch (ffn_mode(P, E)) {
+    case FfnMode::kTiny: return kBlockRowsTiny;
+    case FfnMode::kSmall: return kBlockRows;
+    default: return kBlockRowsLarge;
+  }
 }
 
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
@@ -470,7 +460,18 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
       !make_map(&mH, h, 2, dH, sH, boxRows))
     return cudaErrorInvalidValue;
   cudaError_t err;
-  if (ffn_mode(P, E) == FfnMode::kSmall) {
+  const FfnMode mode = ffn_mode(P, E);
+  if (mode == FfnMode::kTiny) {
+    const long long nb_max = max_blocks(P, E, kBlockRowsTiny);
+    err = launch_gemm<2, true, kBlockRowsTiny, 2>(mW1, mW3, mX, offsets, block_off, num_blocks,
+                                                  block_expert, F, H, nb_max, h, F, status, s);
+    if (err != cudaSuccess) return err;
+    if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
+    return launch_gemm<1, false, kBlockRowsTiny, 2>(mW2, mW2, mH, offsets, block_off,
+                                                    num_blocks, block_expert, H, F, nb_max, y, H,
+                                                    status, s);
+  }
+  if (mode == FfnMode::kSmall) {
     const long long nb_max = max_blocks(P, E, kBlockRows);
     err = launch_gemm<2, true, kBlockRows, 2>(mW1, mW3, mX, offsets, block_off, num_blocks,
                                               block_expert, F, H, nb_max, h, F, status, s);
@@ -507,7 +508,12 @@ cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, 
   const cuuint32_t boxRows[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
   if (!make_map(&mG, Wg, 3, dG, sG, boxW) || !make_map(&mX, x, 2, dX, sX, boxRows))
     return cudaErrorInvalidValue;
-  if (ffn_mode(T, 1) == FfnMode::kSmall)
+  const FfnMode mode = ffn_mode(T, 1);
+  if (mode == FfnMode::kTiny)
+    return launch_gemm<1, false, kBlockRowsTiny, 2, true>(
+        mG, mG, mX, offsets, block_off, num_blocks, block_expert, E, H,
+        max_blocks(T, 1, kBlockRowsTiny), logits, E, status, s);
+  if (mode == FfnMode::kSmall)
     return launch_gemm<1, false, kBlockRows, 2, true>(mG, mG, mX, offsets, block_off, num_blocks,
                                                       block_expert, E, H,
                                                       max_blocks(T, 1, kBlockRows), logits, E,

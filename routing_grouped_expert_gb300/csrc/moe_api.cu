@@ -112,6 +112,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
 
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
   // status word and the chunk histogram table (adjacent) start at zero
+  // status word and the chunk histogram table (adjacent) start at zero
   if (clear)
     MOE_TRY(cudaMemsetAsync(status, 0,
                             L.chunk_base - L.status + (size_t)C * E * sizeof(int32_t), s));
@@ -315,7 +316,9 @@ size_t moe_workspace_size_gated(int T, int H, int F, int Fs, int E, int k) {
 namespace {
 // Router-only workspace: status word, then the single-expert plan.
 constexpr size_t kRouterPlanOffset = 256;
-size_t router_ws_bytes(int T) { return kRouterPlanOffset + 64 + 4 * ((size_t)max_blocks(T, 1) + 1); }
+size_t router_ws_bytes(int T) {
+  return kRouterPlanOffset + 64 + 4 * ((size_t)max_blocks(T, 1, kBlockRowsTiny) + 1);
+}
 SingleExpertPlan router_plan(void* ws) {
   int32_t* p = ws_ptr<int32_t>(ws, kRouterPlanOffset);
   return SingleExpertPlan{p, p + 2, p + 4, p + 16};

@@ -12,12 +12,12 @@
 namespace moe {
 
 // ---------------------------------------------------------------- tiling
-// Token block: at most beta routed rows of one expert.  Each expert's rows
-// are cut into blocks of beta rows, which leaves at most one partial block
-// per expert (MegaFlux, §3.1).  The block is the N side of the expert GEMM
-// tile; the M side is kTileM output features.  beta is 128 when experts get
-// few rows (decode batches) and 256 otherwise; kBlockRows is the smaller one
-// and bounds the number of blocks.
+// Token block: at most beta routed rows of one expert (MegaFlux, §3.1).  The
+// block is the N side of the expert GEMM tile; the M side is kTileM output
+// features.  beta is 64 for decode batches (few rows per expert), 128 for
+// moderate ones and 256 for large ones; block tables are sized for the
+// smallest beta.
+constexpr int kBlockRowsTiny = 64;
 constexpr int kBlockRows = 128;
 constexpr int kBlockRowsLarge = 256;
 constexpr int kTileM = 128;
@@ -25,6 +25,27 @@ constexpr int kTileK = 64;           // one 128-byte swizzle atom of bf16
 constexpr int kRowBox = 32;          // token rows per TMA box of the N operand
 constexpr int kGroupBlocks = 16;     // blocks of one expert rastered together
 
+// Upper bound of the number of token blocks over all experts.
+inline __host__ __device__ long long max_blocks(long long P, int E, int beta = kBlockRows) {
+  const long long nonempty = P < E ? P : E;
+  return (P + beta - 1) / beta + nonempty;
+}
+
+// Tile configuration of the grouped FFN, a function of the routed rows P
+// and the expert count E (mean rows per expert P/E):
+//   tiny  (mean <= 40): 64-row blocks;
+//   small (mean <= 80): 128-row blocks;
+//   large            : 256-row blocks, two weight tiles per CTA tile.
+// With uniform routing the largest expert stays within one block in the
+// tiny and small modes.
+enum class FfnMode { kTiny, kSmall, kLarge };
+constexpr int kTinyModeMeanRows = 40;
+constexpr int kSmallModeMeanRows = 80;
+inline FfnMode ffn_mode(long long P, int E) {
+  if (P <= (long long)kTinyModeMeanRows * E) return FfnMode::kTiny;
+  if (P <= (long long)kSmallModeMeanRows * E) return FfnMode::kSmall;
+  return FfnMode::kLarge;
+}
 // Permute chunking: one CTA handles the assignments of kChunkAssign / k
 // consecutive tokens (at most kChunkAssign assignments).
 constexpr int kChunkAssign = 512;
@@ -32,11 +53,6 @@ inline __host__ __device__ int tokens_per_chunk(int k) { return kChunkAssign / k
 inline __host__ __device__ int num_chunks(int T, int k) {
   const int tpc = tokens_per_chunk(k);
   return (T + tpc - 1) / tpc;
-}
-// Upper bound of the number of token blocks over all experts.
-inline __host__ __device__ long long max_blocks(long long P, int E, int beta = kBlockRows) {
-  const long long nonempty = P < E ? P : E;
-  return (P + beta - 1) / beta + nonempty;
 }
 
 // --------------------------------------------------------- device status
@@ -90,7 +106,6 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   const size_t P = (size_t)T * k;
   const size_t C = (size_t)num_chunks(T, k);
-  const size_t NB = (size_t)max_blocks((long long)P, E);
   WsLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
@@ -104,7 +119,7 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   L.dest_of = take(P * 4);
   L.block_off = take((size_t)(E + 1) * 4);
   L.num_blocks = take(4);
-  L.block_expert = take(NB * 4 + 4);
+  L.block_expert = take((size_t)max_blocks((long long)P, E, kBlockRowsTiny) * 4 + 4);
   L.x_perm = take(P * H * 2);
   L.h = take(P * F * 2);
   L.y = take(P * H * 2);
@@ -124,7 +139,7 @@ inline GatedLayout gated_layout(int T, int H, int F, int Fs, int E, int k) {
   G.s_offsets = take(2 * 4);
   G.s_block_off = take(2 * 4);
   G.s_num_blocks = take(4);
-  G.s_block_expert = take((size_t)max_blocks(T, 1) * 4 + 4);
+  G.s_block_expert = take((size_t)max_blocks(T, 1, kBlockRowsTiny) * 4 + 4);
   G.s_h = take((size_t)T * (Fs > 0 ? Fs : 0) * 2);
   G.s_y = take((size_t)T * H * 2);
   G.total = o;

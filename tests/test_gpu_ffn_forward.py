@@ -24,6 +24,8 @@ CASES = {  # name: (T, H, F, E, k, skew_alpha)
     "k_equals_E": (50, 128, 256, 3, 3, 0.0),
     # > 128 rows per expert: 256-row blocks; F >= 4096 pairs two W2 tiles in FC2
     "large_blocks_paired_fc2": (600, 512, 4096, 2, 2, 0.0),
+    # decode-like (64-row blocks) with a long FC2 K range
+    "decode_long_k": (48, 256, 1024, 8, 2, 0.0),
     # more tokens than a grid's y dimension holds (65535)
     "many_tokens": (70000, 128, 128, 4, 1, 0.0),
 }
@@ -111,3 +113,12 @@ def test_empty_batch_forward():
     out = moe.moe_forward(torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"),
                           torch.empty(0, 4, device="cuda"), W1, W3, W2, 2)
     assert out.shape == (0, 128)
+
+
+def test_fused_and_stepwise_paths_agree_bit_for_bit(case):
+    wl, d, dev, ref = case
+    out = moe.moe_forward(dev["x"], dev["logits"], dev["W1"], dev["W3"], dev["W2"], wl.k)
+    idx, w = moe.moe_route_topk(dev["logits"], wl.k)
+    counts, off, src, dest = moe.moe_permute(idx, wl.E)
+    y = moe.moe_grouped_ffn(dev["x"], src, off, dev["W1"], dev["W3"], dev["W2"], wl.k)
+    assert torch.equal(moe.moe_combine(y, dest, w), out)
