@@ -24,8 +24,9 @@
 // tile, the single-GPU counterpart of replicating a hot expert
 // ("MegaScale-Infer", §3.4 Load Balancing; "MegaFlux", §3.1-3.2).
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
-// TMEM owner, warps 2-5 = epilogue (TMEM -> registers -> global).  Shared
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 2-9 = epilogue (TMEM -> registers -> global): two warps
+// per TMEM lane quadrant, taking alternate 16-column chunks.  Shared
 // memory holds a ring of operand stages; where TMEM has room for two
 // accumulator buffers the epilogue of one tile overlaps the MMAs of the
 // next.  Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT
@@ -45,7 +46,8 @@ constexpr int BK = kTileK;          // K per pipeline stage
 constexpr int kAHalfBytes = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
 constexpr int kABytes = BM * BK * 2;              // 16 KB per weight tile per stage
 constexpr int kBBoxBytes = kRowBox * BK * 2;      // 32 token rows: 4 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 204800;               // operand ring: 200 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
@@ -143,7 +145,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&bars->acc_full[b], 1);
-      mbar_init(&bars->acc_empty[b], 4);   // one arrival per epilogue warp
+      mbar_init(&bars->acc_empty[b], kEpiWarps);   // one arrival per epilogue warp
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -279,7 +281,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;   // TMEM lane quadrant this warp may read
+    const int q = warp & 3;            // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;  // which alternate 16-column chunks it takes
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -298,7 +301,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         // zero padding and are not stored.
         float* col = static_cast<float*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
         const bool store = feat < m_valid;
-        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+        for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
           uint32_t g[16];
           tmem_ld_32x32b_x16(tb + c0, g);
           tmem_ld_wait();
@@ -309,7 +312,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       } else {
       __nv_bfloat16* col =
           static_cast<__nv_bfloat16*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
-      for (int c0 = 0; c0 < it.nrows; c0 += 16) {
+      for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
         uint32_t g[16];
         tmem_ld_32x32b_x16(tb + c0, g);
         if constexpr (kGLU) {
