@@ -35,6 +35,21 @@ Sources for each step:
   weighted top-k sum back to token order:
       "MegaFlux", §2.1; "MegaScale-Infer", §3.2 step (4)-(5).
 
+Backward ("backward"): the gradients of the layer output with respect to x,
+the router logits and the three expert matrices, given dout = dL/dout --
+the DGrad/WGrad streams of the backward MoE pass ("MegaFlux", §2.1 and
+§3.2 backward).  Written from the chain rule of the forward above:
+  dY_p   = w[t,j] dout[t]                      (combine, p = dest_of[t*k+j])
+  dw_tj  = <dout[t], y_p>                       (routing weight)
+  dW2[e] = h_e^T dY_e,  dh = dY W2[e]^T        (FC2 WGrad / DGrad)
+  dg = dh * u * s * (1 + g (1 - s)),  du = dh * g * s,  s = sigmoid(g)
+  dW1[e] = x_e^T dg,  dW3[e] = x_e^T du,  dx_p = dg W1[e]^T + du W3[e]^T
+  dx[t]  = sum_j dx_p                           (scatter back to tokens)
+  dlogits[t, e_j] = w_j (dw_j - sum_i w_i dw_i), zero for unselected experts
+                                                (softmax over the k selected).
+The forward uses the fp32-rounded weights w; the logit gradient applies the
+exact (fp64) softmax Jacobian, treating that rounding as the identity.
+
 Either side of the routed path ("forward_gated"):
   router projection: the gating network that decides each token's experts
       ("MegaScale-Infer", §3.2 Big-Picture Architecture, item 2; "Piper",
@@ -267,3 +282,56 @@ def forward_gated(x, Wg, W1, W3, W2, k: int, shared=None, logits=None):
         r["shared"] = expert_ffn(x, *shared)
         r["out"] = r["out"] + r["shared"]
     return r
+
+
+# --------------------------------------------------------------------------
+# Backward of the layer
+# --------------------------------------------------------------------------
+def backward(x, logits, W1, W3, W2, k: int, dout):
+    """Gradients of out = forward_perm(...)["out"] for the upstream gradient
+    dout [T, H].  Returns dict with dx [T, H], dlogits [T, E], dW1, dW3
+    [E, H, F], dW2 [E, F, H] and dw [T, k] (gradient of the routing
+    weights), all fp64."""
+    l = np.asarray(logits, dtype=np.float32)
+    T, E = l.shape
+    idx, w = route_topk(l, k)
+    counts, offsets, sorted_src, dest_of = permute(idx, E)
+    x64, d64 = _f64(x), _f64(dout)
+    H = x64.shape[1]
+    w64 = w.astype(np.float64)
+    dx = np.zeros((T, H))
+    dw = np.zeros((T, k))
+    grads = {"dW1": [], "dW3": [], "dW2": []}
+    for e in range(E):
+        W1e, W3e, W2e = _f64(W1[e]), _f64(W3[e]), _f64(W2[e])
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        a = sorted_src[lo:hi]
+        t, j = a // k, a % k
+        if lo == hi:
+            grads["dW1"].append(np.zeros_like(W1e))
+            grads["dW3"].append(np.zeros_like(W3e))
+            grads["dW2"].append(np.zeros_like(W2e))
+            continue
+        X = x64[t]
+        g, u = _mm(X, W1e), _mm(X, W3e)
+        s = 1.0 / (1.0 + np.exp(-g))
+        h = g * s * u
+        Y = _mm(h, W2e)
+        dY = w64[t, j][:, None] * d64[t]
+        dw[t, j] = np.sum(d64[t] * Y, axis=1)
+        grads["dW2"].append(_mm(h.T, dY))
+        dh = _mm(dY, W2e.T)
+        dg = dh * u * s * (1.0 + g * (1.0 - s))
+        du = dh * g * s
+        grads["dW1"].append(_mm(X.T, dg))
+        grads["dW3"].append(_mm(X.T, du))
+        np.add.at(dx, t, _mm(dg, W1e.T) + _mm(du, W3e.T))
+    # exact softmax of the selected logits for the Jacobian
+    sel = np.take_along_axis(l.astype(np.float64), idx.astype(np.int64), axis=1)
+    ex = np.exp(sel - sel[:, :1])
+    p_exact = ex / ex.sum(axis=1, keepdims=True)
+    dsel = p_exact * (dw - np.sum(p_exact * dw, axis=1, keepdims=True))
+    dlogits = np.zeros((T, E))
+    np.put_along_axis(dlogits, idx.astype(np.int64), dsel, axis=1)
+    return dict(dx=dx, dlogits=dlogits, dw=dw, dW1=np.stack(grads["dW1"]),
+                dW3=np.stack(grads["dW3"]), dW2=np.stack(grads["dW2"]))

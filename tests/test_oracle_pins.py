@@ -270,6 +270,85 @@ def test_shared_expert_adds_the_dense_ffn():
     np.testing.assert_allclose(r0["out"], dense.numpy(), rtol=1e-12, atol=1e-12)
 
 
+# --------------------------------------------------------------- backward
+def autograd_grads(x, logits, W1, W3, W2, k, dout):
+    """The same layer written as plain torch fp64 ops with the top-k picks
+    held fixed, differentiated by torch.autograd."""
+    idx, _ = O.route_topk(np.asarray(logits, np.float32), k)
+    idx_t = torch.as_tensor(idx, dtype=torch.long)
+    xt = torch.as_tensor(np.asarray(x, np.float64)).requires_grad_()
+    lt = torch.as_tensor(np.asarray(logits, np.float32).astype(np.float64)).requires_grad_()
+    Ws = [torch.as_tensor(np.asarray(W, np.float64)).requires_grad_() for W in (W1, W3, W2)]
+    w = torch.softmax(torch.gather(lt, 1, idx_t), dim=1)
+    # the layer uses fp32-rounded weights; the rounding passes gradients through
+    w = w + (w.float().double() - w).detach()
+    out = torch.zeros_like(xt)
+    for j in range(k):
+        e = idx_t[:, j]
+        g = torch.einsum("th,thf->tf", xt, Ws[0][e])
+        u = torch.einsum("th,thf->tf", xt, Ws[1][e])
+        y = torch.einsum("tf,tfh->th", torch.nn.functional.silu(g) * u, Ws[2][e])
+        out = out + w[:, j:j + 1] * y
+    (out * torch.as_tensor(np.asarray(dout, np.float64))).sum().backward()
+    return dict(dx=xt.grad.numpy(), dlogits=lt.grad.numpy(), dW1=Ws[0].grad.numpy(),
+                dW3=Ws[1].grad.numpy(), dW2=Ws[2].grad.numpy())
+
+
+def check_backward_autograd(backward=None, seed=21):
+    backward = backward or O.backward
+    rng = np.random.default_rng(seed)
+    T, H, F, E, k = 9, 4, 6, 5, 2
+    x = rng.standard_normal((T, H))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    W1, W3 = rng.standard_normal((E, H, F)) / 2, rng.standard_normal((E, H, F)) / 2
+    W2 = rng.standard_normal((E, F, H)) / 2
+    dout = rng.standard_normal((T, H))
+    got = backward(x, logits, W1, W3, W2, k, dout)
+    want = autograd_grads(x, logits, W1, W3, W2, k, dout)
+    for name in ("dx", "dlogits", "dW1", "dW3", "dW2"):
+        np.testing.assert_allclose(got[name], want[name], rtol=1e-10, atol=1e-12, err_msg=name)
+
+
+def test_backward_matches_autograd():
+    check_backward_autograd()
+
+
+def test_backward_finite_differences():
+    """Central differences of L = <dout, out> for a few entries of each input."""
+    rng = np.random.default_rng(22)
+    T, H, F, E, k = 6, 3, 5, 4, 2
+    args = dict(x=rng.standard_normal((T, H)), logits=rng.standard_normal((T, E)),
+                W1=rng.standard_normal((E, H, F)), W3=rng.standard_normal((E, H, F)),
+                W2=rng.standard_normal((E, F, H)))
+    dout = rng.standard_normal((T, H))
+
+    def loss(a):
+        return float(np.sum(dout * O.forward_perm(a["x"], a["logits"], a["W1"], a["W3"],
+                                                  a["W2"], k)["out"]))
+
+    g = O.backward(args["x"], args["logits"], args["W1"], args["W3"], args["W2"], k, dout)
+    top = int(np.argmax(args["logits"][4]))
+    # logits are ranked and weighted in fp32: a step well above fp32 resolution
+    for name, key, pos, eps, tol in (("x", "dx", (2, 1), 1e-6, 1e-6),
+                                     ("W1", "dW1", (1, 2, 3), 1e-6, 1e-6),
+                                     ("W3", "dW3", (0, 1, 4), 1e-6, 1e-6),
+                                     ("W2", "dW2", (3, 4, 0), 1e-6, 1e-6),
+                                     ("logits", "dlogits", (4, top), 1e-3, 2e-3)):
+        plus = {n: v.copy() for n, v in args.items()}
+        minus = {n: v.copy() for n, v in args.items()}
+        plus[name][pos] += eps
+        minus[name][pos] -= eps
+        fd = (loss(plus) - loss(minus)) / (2 * eps)
+        assert abs(fd - g[key][pos]) <= tol * max(1.0, abs(fd)), (name, fd, g[key][pos])
+
+
+def test_backward_top1_has_no_logit_gradient():
+    x, logits, W1, W3, W2 = rand_layer(20, 8, 12, 4, 1, seed=23)
+    dout = np.random.default_rng(24).standard_normal((20, 8))
+    g = O.backward(x, logits, W1, W3, W2, 1, dout)
+    assert np.all(g["dlogits"] == 0)
+
+
 # ------------------------------------------------- the pages' own numbers
 def test_util_formula_a100_example():
     g = json.load(open(os.path.join(GOLDEN, "util_a100_example.json")))
@@ -358,6 +437,21 @@ def test_pins_catch_planted_mistakes():
         return counts, offsets, src, dest
     with pytest.raises(AssertionError):
         check_permute(permute_rev)
+
+    # 8. a weight gradient off by a tenth of a percent
+    def backward_bad(x, logits, W1, W3, W2, k, dout):
+        g = O.backward(x, logits, W1, W3, W2, k, dout)
+        g["dW1"] = g["dW1"] * 1.001
+        return g
+    with pytest.raises(AssertionError):
+        check_backward_autograd(backward_bad)
+
+    # 9. the routing weights left out of dY (dY = dout)
+    def backward_unweighted(x, logits, W1, W3, W2, k, dout):
+        ones = np.zeros_like(np.asarray(logits, np.float32))
+        return O.backward(x, ones, W1, W3, W2, k, dout)
+    with pytest.raises(AssertionError):
+        check_backward_autograd(backward_unweighted)
 
     # 7. router computed with the transposed product
     with pytest.raises((AssertionError, ValueError, RuntimeError)):
