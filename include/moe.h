@@ -230,6 +230,36 @@ moe_status moe_forward_gated(const void* x, const void* Wg,
                              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Training: the layer's backward ("MegaFlux" §2.1 and §3.2: the backward
+ * streams token blocks through DGrad and WGrad grouped GEMMs; the final
+ * top-k sum's gradient gives each routing weight's gradient).
+ *
+ * moe_forward_train is moe_forward that also keeps, in `ws`, what the
+ * backward needs (routing, gathered x rows, the gate and up pre-activations
+ * g = x W1 and u = x W3 in bf16, h and the expert outputs); ws must hold
+ * moe_workspace_size_train bytes.  moe_backward then takes dout = dL/dout
+ * [T, H] bf16 and the same logits and weights, and writes
+ *   dx      [T, H] bf16,
+ *   dlogits [T, E] fp32 (softmax Jacobian over the k selected logits;
+ *           zero for unselected experts),
+ *   dW1, dW3 [E, H, F] bf16, dW2 [E, F, H] bf16 (fp32 accumulation; zero
+ *           for experts that received no token).
+ * The two calls must use the same ws, sizes, logits and weights, with no
+ * other call on that ws in between; moe_backward leaves the saved state
+ * intact, so it may be repeated (e.g. for another dout).
+ */
+size_t moe_workspace_size_train(int T, int H, int F, int E, int k);
+moe_status moe_forward_train(const void* x, const float* router_logits,
+                             const void* W1, const void* W3, const void* W2,
+                             int T, int H, int F, int E, int k, void* out,
+                             void* ws, size_t ws_bytes, void* stream);
+moe_status moe_backward(const void* dout, const float* router_logits,
+                        const void* W1, const void* W3, const void* W2,
+                        int T, int H, int F, int E, int k,
+                        void* dx, float* dlogits, void* dW1, void* dW3, void* dW2,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_forward with timing marks: records events[0] on `stream` before the
  * first kernel and events[i] after stage i, for the MOE_FORWARD_STAGES
  * stages route, scan, scatter, gather, fc1, fc2, combine (in that order).

@@ -287,11 +287,18 @@ def forward_gated(x, Wg, W1, W3, W2, k: int, shared=None, logits=None):
 # --------------------------------------------------------------------------
 # Backward of the layer
 # --------------------------------------------------------------------------
-def backward(x, logits, W1, W3, W2, k: int, dout):
+def backward(x, logits, W1, W3, W2, k: int, dout, magnitudes: bool = False):
     """Gradients of out = forward_perm(...)["out"] for the upstream gradient
     dout [T, H].  Returns dict with dx [T, H], dlogits [T, E], dW1, dW3
     [E, H, F], dW2 [E, F, H] and dw [T, k] (gradient of the routing
-    weights), all fp64."""
+    weights), all fp64.
+
+    With magnitudes=True it also returns, under "mag_<name>", the first-order
+    size, in units of eps, of the change that rounding the stored operands
+    (dY, g, u, h, dg, du) by a relative eps makes to each gradient: sums over
+    absolute values that follow each rounding through the chain rule, e.g.
+    for dW1 the rounding of dY through dh, of u, of g through the SwiGLU
+    derivative (whose factor crosses zero near g = -1.28), and of dg."""
     l = np.asarray(logits, dtype=np.float32)
     T, E = l.shape
     idx, w = route_topk(l, k)
@@ -302,15 +309,18 @@ def backward(x, logits, W1, W3, W2, k: int, dout):
     dx = np.zeros((T, H))
     dw = np.zeros((T, k))
     grads = {"dW1": [], "dW3": [], "dW2": []}
+    mag = {"dW1": [], "dW3": [], "dW2": []}
+    mdx = np.zeros((T, H))
+    mdw = np.zeros((T, k))
     for e in range(E):
         W1e, W3e, W2e = _f64(W1[e]), _f64(W3[e]), _f64(W2[e])
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         a = sorted_src[lo:hi]
         t, j = a // k, a % k
         if lo == hi:
-            grads["dW1"].append(np.zeros_like(W1e))
-            grads["dW3"].append(np.zeros_like(W3e))
-            grads["dW2"].append(np.zeros_like(W2e))
+            for name, like in (("dW1", W1e), ("dW3", W3e), ("dW2", W2e)):
+                grads[name].append(np.zeros_like(like))
+                mag[name].append(np.zeros_like(like))
             continue
         X = x64[t]
         g, u = _mm(X, W1e), _mm(X, W3e)
@@ -326,6 +336,22 @@ def backward(x, logits, W1, W3, W2, k: int, dout):
         grads["dW1"].append(_mm(X.T, dg))
         grads["dW3"].append(_mm(X.T, du))
         np.add.at(dx, t, _mm(dg, W1e.T) + _mm(du, W3e.T))
+        if magnitudes:
+            # first-order sizes of what rounding each stored operand by a
+            # relative eps does to each gradient, in units of eps
+            aX, ah, adY = np.abs(X), np.abs(h), np.abs(dY)
+            f = s * (1.0 + g * (1.0 - s))                       # d silu / d g
+            fp = s * (1.0 - s) * (2.0 + g * (1.0 - 2.0 * s))    # its derivative
+            gsp = s + g * s * (1.0 - s)                         # d (g s) / d g
+            m_dh = _mm(adY, np.abs(W2e).T)                      # dY rounding -> dh
+            m_dg = (m_dh * np.abs(u * f) + np.abs(dh * u) * (np.abs(f) + np.abs(g * fp))
+                    + np.abs(dg))
+            m_du = m_dh * np.abs(g * s) + np.abs(dh * g * gsp) + np.abs(du)
+            mag["dW1"].append(_mm(aX.T, m_dg))
+            mag["dW3"].append(_mm(aX.T, m_du))
+            mag["dW2"].append(_mm(ah.T, adY))
+            np.add.at(mdx, t, _mm(m_dg, np.abs(W1e).T) + _mm(m_du, np.abs(W3e).T))
+            mdw[t, j] = np.sum(np.abs(d64[t]) * _mm(ah, np.abs(W2e)), axis=1)
     # exact softmax of the selected logits for the Jacobian
     sel = np.take_along_axis(l.astype(np.float64), idx.astype(np.int64), axis=1)
     ex = np.exp(sel - sel[:, :1])
@@ -333,5 +359,12 @@ def backward(x, logits, W1, W3, W2, k: int, dout):
     dsel = p_exact * (dw - np.sum(p_exact * dw, axis=1, keepdims=True))
     dlogits = np.zeros((T, E))
     np.put_along_axis(dlogits, idx.astype(np.int64), dsel, axis=1)
-    return dict(dx=dx, dlogits=dlogits, dw=dw, dW1=np.stack(grads["dW1"]),
-                dW3=np.stack(grads["dW3"]), dW2=np.stack(grads["dW2"]))
+    r = dict(dx=dx, dlogits=dlogits, dw=dw, dW1=np.stack(grads["dW1"]),
+             dW3=np.stack(grads["dW3"]), dW2=np.stack(grads["dW2"]))
+    if magnitudes:
+        msel = p_exact * (mdw + np.sum(p_exact * mdw, axis=1, keepdims=True))
+        mdl = np.zeros((T, E))
+        np.put_along_axis(mdl, idx.astype(np.int64), msel, axis=1)
+        r.update(mag_dx=mdx, mag_dlogits=mdl, mag_dW1=np.stack(mag["dW1"]),
+                 mag_dW3=np.stack(mag["dW3"]), mag_dW2=np.stack(mag["dW2"]))
+    return r

@@ -15,6 +15,9 @@ from .binding import (  # noqa: F401
     moe_forward_stage_name,
     FORWARD_STAGES,
     moe_forward_host,
+    moe_forward_train,
+    moe_backward,
+    moe_workspace_size_train,
     moe_forward_gated,
     moe_router_logits,
     moe_workspace_size_gated,

@@ -37,6 +37,10 @@ SIGNATURES = {
     "moe_get_device_status": (_I, [_VP, _VP]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_diag_wait_timeout": (_I, [_VP, _SZ, ctypes.c_longlong, _VP]),
+    "moe_workspace_size_train": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_forward_train": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_backward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP,
+                          _VP, _SZ, _VP]),
     "moe_router_logits": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "moe_workspace_size_gated": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_gated": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
@@ -325,3 +329,44 @@ def moe_forward_gated(x, Wg, W1, W3, W2, k: int, shared=None, out=None,
                                             F, Fs, E, k, _p(out), ws.ptr, ws.nbytes, _stream()),
            "moe_forward_gated")
     return out
+
+
+# ------------------------------------------------------------- training
+def moe_workspace_size_train(T: int, H: int, F: int, E: int, k: int) -> int:
+    return int(load_library().moe_workspace_size_train(T, H, F, E, k))
+
+
+def moe_forward_train(x, router_logits, W1, W3, W2, k: int, ws: Workspace, out=None):
+    """moe_forward that keeps in `ws` what moe_backward needs."""
+    T, H = x.shape
+    E, _, F = W1.shape
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_logits, torch.float32, (T, E), "router_logits")
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
+    ws.ensure(moe_workspace_size_train(T, H, F, E, k))
+    _check(load_library().moe_forward_train(_p(x), _p(router_logits), _p(W1), _p(W3), _p(W2),
+                                            T, H, F, E, k, _p(out), ws.ptr, ws.nbytes,
+                                            _stream()), "moe_forward_train")
+    return out
+
+
+def moe_backward(dout, router_logits, W1, W3, W2, k: int, ws: Workspace):
+    """Gradients after moe_forward_train on the same ws: (dx, dlogits, dW1,
+    dW3, dW2)."""
+    T, H = dout.shape
+    E, _, F = W1.shape
+    _need(dout, torch.bfloat16, (T, H), "dout")
+    _need(router_logits, torch.float32, (T, E), "router_logits")
+    dev = dout.device
+    dx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    dl = torch.empty(T, E, dtype=torch.float32, device=dev)
+    dW1 = torch.empty(E, H, F, dtype=torch.bfloat16, device=dev)
+    dW3 = torch.empty(E, H, F, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(E, F, H, dtype=torch.bfloat16, device=dev)
+    _check(load_library().moe_backward(_p(dout), _p(router_logits), _p(W1), _p(W3), _p(W2), T, H,
+                                       F, E, k, _p(dx), _p(dl), _p(dW1), _p(dW3), _p(dW2),
+                                       ws.ptr, ws.nbytes, _stream()), "moe_backward")
+    return dx, dl, dW1, dW3, dW2

@@ -30,7 +30,7 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = dest_of[(size_t)t * k + threadIdx.x];
-    s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = topk_w ? topk_w[(size_t)t * k + threadIdx.x] : 1.0f;   // null: unweighted
   }
   __syncthreads();
   const int nv = H / 8;

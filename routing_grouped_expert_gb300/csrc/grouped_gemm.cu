@@ -51,13 +51,25 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 204800;               // operand ring: 200 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
-// kNumA weight tiles of 128 rows share each token block:
-//   FC1 (kGLU): gate and up tiles of the same 128 features;
-//   FC2 with kNumA = 2: two adjacent 128-feature tiles of W2.
-// kBN = token rows per block (beta), kAccBufs = TMEM accumulator buffers,
-// kOutF32 = fp32 output (router logits) instead of bf16.
-template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32 = false>
+// What the epilogue does with the fp32 accumulators.
+enum : int {
+  kEpiBf16 = 0,        // out = acc (bf16); kNumA = 2: two adjacent 128-feature tiles
+  kEpiSwiglu = 1,      // out = silu(acc0) * acc1 (bf16): FC1
+  kEpiSwigluSave = 2,  // as kEpiSwiglu, and g = acc0, u = acc1 kept (bf16) for the backward
+  kEpiF32 = 3,         // out = acc (fp32); features >= m_valid not stored: router logits
+  kEpiSwigluBwd = 4,   // acc = dh: dg = dh*u*s*(1 + g(1 - s)), du = dh*g*s, s = sigmoid(g)
+};
+
+// kNumA weight tiles of 128 rows share each token block (FC1: gate and up of
+// the same features; FC2 with kNumA = 2: two adjacent feature tiles).
+// kBN = token rows per block, kAccBufs = TMEM accumulator buffers.
+// kAKMajor: the weight tile is read K-major (the backward's W^T products)
+// instead of MN-major.  kDualK: the K loop runs twice, first over
+// (A0, B0) then over (A1, B1), into one accumulator (dx = dg W1^T + du W3^T).
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false,
+          bool kDualK = false>
 struct Cfg {
+  static constexpr bool kGLU = kEpi == kEpiSwiglu || kEpi == kEpiSwigluSave;
   static constexpr int kBBytes = kBN * BK * 2;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
@@ -69,7 +81,8 @@ struct Cfg {
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
-  static_assert(!kOutF32 || (kNumA == 1 && !kGLU), "fp32 output: single plain tile");
+  static_assert((kEpi != kEpiF32 && kEpi != kEpiSwigluBwd) || kNumA == 1, "single tile");
+  static_assert(!kDualK || (kNumA == 1 && kAKMajor), "two-phase K: one K-major tile");
 };
 
 struct Bars {
@@ -119,24 +132,27 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   return it;
 }
 
-template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32>
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB1,
                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ block_off,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
-                    void* __restrict__ out_ptr, int ld_out, int m_valid,
+                    void* __restrict__ out_ptr, int ld_out, int m_valid, EpiAux aux,
                     int* __restrict__ status) {
-  using C = Cfg<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
+  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  constexpr bool kGLU = C::kGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = *num_blocks_ptr * n_mt;
-  const int nkb = K / BK;
+  const int nkb = K / BK;                        // K stages per phase
+  const int nkb_all = kDualK ? 2 * nkb : nkb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -153,8 +169,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA0);
-    if (kGLU) prefetch_tmap(&tmA1);
+    if (kGLU || kDualK) prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
+    if (kDualK) prefetch_tmap(&tmB1);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -184,25 +201,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         const uint32_t bytes = kNumA * kABytes + nbox * kBBoxBytes;
         const int f0 = it.mt * C::kFeatPerItem;
         const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb_all; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
+          const bool second = kDualK && kb >= nkb;    // second K phase
+          const int k0 = (second ? kb - nkb : kb) * BK;
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + kNumA * kABytes;
           uint64_t* fb = &bars->full[stage];
-          const int k0 = kb * BK;
           mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
           for (int a = 0; a < kNumA; ++a) {
-            const CUtensorMap* map = (kGLU && a == 1) ? &tmA1 : &tmA0;
+            const CUtensorMap* map = ((kGLU && a == 1) || second) ? &tmA1 : &tmA0;
             const int fa = f0 + (kGLU ? 0 : a * BM);
-            tma_load_3d(sA + a * kABytes, map, fb, fa, k0, it.e, pol_w);
-            tma_load_3d(sA + a * kABytes + kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
+            if constexpr (kAKMajor) {
+              // 128 weight rows x 64 K, K contiguous: one box
+              tma_load_3d(sA + a * kABytes, map, fb, k0, fa, it.e, pol_w);
+            } else {
+              // 64 K rows x 64 features per box, features contiguous: two boxes
+              tma_load_3d(sA + a * kABytes, map, fb, fa, k0, it.e, pol_w);
+              tma_load_3d(sA + a * kABytes + kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
+            }
           }
+          const CUtensorMap* bmap = second ? &tmB1 : &tmB;
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sB + bx * kBBoxBytes, &tmB, fb, k0, it.row0 + bx * kRowBox, pol_x);
+            tma_load_2d(sB + bx * kBBoxBytes, bmap, fb, k0, it.row0 + bx * kRowBox, pol_x);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -229,14 +254,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int n = (it.nrows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(BM, n, /*a_mn=*/true, /*b_mn=*/false);
+        const uint32_t idesc = idesc_bf16(BM, n, /*a_mn=*/!kAKMajor, /*b_mn=*/false);
         if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb_all; ++kb) {
           if (!mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -249,13 +274,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             // N operand: K-major rows of 128 B; K step of 16 = 32 B inside the atom.
             const uint64_t db = sdesc_sw128(b0 + kk * 32, 16, 1024);
-            // M operand: MN-major; 64-feature atoms 8 KB apart (LBO), 8 K-rows
-            // per 1 KB group (SBO); K step of 16 = 16 rows = 2 KB.
 #pragma unroll
-            for (int a = 0; a < kNumA; ++a)
-              mma_bf16_ss(d0 + (uint32_t)(a * kBN),
-                          sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024), db,
-                          idesc, accum);
+            for (int a = 0; a < kNumA; ++a) {
+              // M operand.  MN-major: 64-feature atoms 8 KB apart (LBO), 8 K-rows
+              // per 1 KB group (SBO), K step of 16 = 16 rows = 2 KB.  K-major:
+              // rows of 128 B, 8-row groups 1 KB apart, K step of 16 = 32 B.
+              const uint64_t da =
+                  kAKMajor ? sdesc_sw128(a0 + a * kABytes + kk * 32, 16, 1024)
+                           : sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024);
+              mma_bf16_ss(d0 + (uint32_t)(a * kBN), da, db, idesc, accum);
+            }
           }
           mma_commit(&bars->empty[stage]);
           if (++stage == C::kStages) {
@@ -296,56 +324,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       tc_fence_after();
       const int feat = it.mt * C::kFeatPerItem + q * 32 + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      if constexpr (kOutF32) {
-        // fp32 output; rows of a partial weight tile (feature >= m_valid) are
-        // zero padding and are not stored.
-        float* col = static_cast<float*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
-        const bool store = feat < m_valid;
-        for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
-          uint32_t g[16];
-          tmem_ld_32x32b_x16(tb + c0, g);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (store && c0 + c < it.nrows) col[(size_t)(c0 + c) * ld_out] = __uint_as_float(g[c]);
-        }
-      } else {
-      __nv_bfloat16* col =
-          static_cast<__nv_bfloat16*>(out_ptr) + (size_t)it.row0 * ld_out + feat;
       for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
-        uint32_t g[16];
+        uint32_t g[16], g2[16];
         tmem_ld_32x32b_x16(tb + c0, g);
-        if constexpr (kGLU) {
-          uint32_t u[16];
-          tmem_ld_32x32b_x16(tb + kBN + c0, u);
-          tmem_ld_wait();
+        if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
+        tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c < it.nrows) {
-              const float gv = __uint_as_float(g[c]);
-              const float hv = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
-              col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(hv);
+        for (int c = 0; c < 16; ++c) {
+          if (c0 + c >= it.nrows) continue;
+          const size_t row = (size_t)(it.row0 + c0 + c);
+          const float a0 = __uint_as_float(g[c]);
+          if constexpr (kEpi == kEpiF32) {
+            // rows of a partial weight tile (feature >= m_valid) are zero padding
+            if (feat < m_valid) static_cast<float*>(out_ptr)[row * ld_out + feat] = a0;
+          } else if constexpr (kGLU) {
+            const float a1 = __uint_as_float(g2[c]);
+            const float hv = __fdividef(a0 * a1, 1.0f + __expf(-a0));
+            static_cast<__nv_bfloat16*>(out_ptr)[row * ld_out + feat] = __float2bfloat16_rn(hv);
+            if constexpr (kEpi == kEpiSwigluSave) {
+              aux.g[row * aux.ld + feat] = __float2bfloat16_rn(a0);
+              aux.u[row * aux.ld + feat] = __float2bfloat16_rn(a1);
             }
+          } else if constexpr (kEpi == kEpiSwigluBwd) {
+            const float gv = __bfloat162float(aux.g[row * aux.ld + feat]);
+            const float uv = __bfloat162float(aux.u[row * aux.ld + feat]);
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+            aux.dg[row * aux.ld + feat] =
+                __float2bfloat16_rn(a0 * uv * sg * (1.0f + gv * (1.0f - sg)));
+            aux.du[row * aux.ld + feat] = __float2bfloat16_rn(a0 * gv * sg);
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out_ptr) + row * ld_out + feat;
+            o[0] = __float2bfloat16_rn(a0);
+            if constexpr (kNumA == 2) o[BM] = __float2bfloat16_rn(__uint_as_float(g2[c]));
           }
-        } else if constexpr (kNumA == 2) {
-          uint32_t g2[16];
-          tmem_ld_32x32b_x16(tb + kBN + c0, g2);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c < it.nrows) {
-              col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(__uint_as_float(g[c]));
-              col[(size_t)(c0 + c) * ld_out + BM] = __float2bfloat16_rn(__uint_as_float(g2[c]));
-            }
-          }
-        } else {
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (c0 + c < it.nrows)
-              col[(size_t)(c0 + c) * ld_out] = __float2bfloat16_rn(__uint_as_float(g[c]));
         }
-      }
       }
       tc_fence_before();
       __syncwarp();
@@ -399,14 +411,26 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kNumA, bool kGLU, int kBN, int kAccBufs, bool kOutF32 = false>
+}  // namespace
+
+bool make_tensor_map_bf16(void* map, const void* base, int rank, const unsigned long long* dims,
+                          const unsigned long long* strides, const unsigned int* box) {
+  return make_map(static_cast<CUtensorMap*>(map), base, rank,
+                  reinterpret_cast<const cuuint64_t*>(dims),
+                  reinterpret_cast<const cuuint64_t*>(strides),
+                  reinterpret_cast<const cuuint32_t*>(box));
+}
+
+namespace {
+
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false, bool kDualK = false>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const int32_t* offsets, const int32_t* block_off,
+                        const CUtensorMap& b1, const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
-                        int K, long long nb_max, void* out, int ld_out, int* status,
-                        cudaStream_t s) {
-  using C = Cfg<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
-  auto kern = grouped_gemm_kernel<kNumA, kGLU, kBN, kAccBufs, kOutF32>;
+                        int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
+                        int* status, cudaStream_t s) {
+  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -415,8 +439,8 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   const int n_mt = (M_total + C::kFeatPerItem - 1) / C::kFeatPerItem;
   const long long items = nb_max * n_mt;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, offsets, block_off, num_blocks,
-                                             block_expert, n_mt, K, out, ld_out, M_total,
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, b1, offsets, block_off, num_blocks,
+                                             block_expert, n_mt, K, out, ld_out, M_total, aux,
                                              status);
   return cudaGetLastError();
 }
@@ -427,6 +451,78 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 #define MOE_FC2_PAIR_MIN_F 0
 #endif
 bool fc2_paired(int H, int F) { return H % (2 * BM) == 0 && F >= MOE_FC2_PAIR_MIN_F; }
+
+struct PlanPtrs {
+  const int32_t* offsets;
+  const int32_t* block_off;
+  const int32_t* num_blocks;
+  const int32_t* block_expert;
+};
+
+// Weights as the MN-major M operand ([E, K, M] memory, M contiguous): boxes of
+// 64 features x 64 K rows.
+bool map_weights_mn(CUtensorMap* m, const void* W, int K, int M, int E) {
+  const cuuint64_t d[3] = {(cuuint64_t)M, (cuuint64_t)K, (cuuint64_t)E};
+  const cuuint64_t st[2] = {(cuuint64_t)M * 2, (cuuint64_t)K * M * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)BK, 1};
+  return make_map(m, W, 3, d, st, box);
+}
+// Weights as the K-major M operand ([E, M, K] memory, K contiguous): boxes of
+// 128 rows x 64 K.
+bool map_weights_k(CUtensorMap* m, const void* W, int M, int K, int E) {
+  const cuuint64_t d[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)E};
+  const cuuint64_t st[2] = {(cuuint64_t)K * 2, (cuuint64_t)M * K * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1};
+  return make_map(m, W, 3, d, st, box);
+}
+// Token rows [P, K] (K contiguous) as the N operand: boxes of 32 rows x 64 K.
+bool map_rows(CUtensorMap* m, const void* X, int K, int P) {
+  const cuuint64_t d[2] = {(cuuint64_t)K, (cuuint64_t)P};
+  const cuuint64_t st[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
+  return make_map(m, X, 2, d, st, box);
+}
+
+template <int kBN, int kBufs1>
+cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUtensorMap& mX,
+                       const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
+                       const EpiAux* save, int* status, cudaStream_t s) {
+  const long long nb_max = max_blocks(P, E, kBN);
+  if (save != nullptr)
+    return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
+                                                       pl.num_blocks, pl.block_expert, F, H,
+                                                       nb_max, h, F, *save, status, s);
+  return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
+                                                 pl.num_blocks, pl.block_expert, F, H, nb_max, h,
+                                                 F, EpiAux{}, status, s);
+}
+
+template <int kNumA, int kBN, int kBufs>
+cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const PlanPtrs& pl, int P,
+                       int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s) {
+  return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(mW2, mW2, mH, mH, pl.offsets, pl.block_off,
+                                                  pl.num_blocks, pl.block_expert, H, F,
+                                                  max_blocks(P, E, kBN), y, H, EpiAux{}, status,
+                                                  s);
+}
+
+template <int kBN>
+cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
+                           const CUtensorMap& mW1k, const CUtensorMap& mW3k,
+                           const CUtensorMap& mDG, const CUtensorMap& mDU, const PlanPtrs& pl,
+                           int P, int H, int F, int E, const EpiAux& aux,
+                           __nv_bfloat16* dx_perm, int* status, cudaStream_t s) {
+  const long long nb_max = max_blocks(P, E, kBN);
+  // dh = dY W2[e]^T (M = F, K = H), then the SwiGLU derivative -> dg, du
+  cudaError_t err = launch_gemm<1, kEpiSwigluBwd, kBN, 2, true>(
+      mW2k, mW2k, mDY, mDY, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H,
+      nb_max, nullptr, 0, aux, status, s);
+  if (err != cudaSuccess) return err;
+  // dx_perm = dg W1[e]^T + du W3[e]^T (M = H, K = F in two phases)
+  return launch_gemm<1, kEpiBf16, kBN, 2, true, true>(
+      mW1k, mW3k, mDG, mDU, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
+      nb_max, dx_perm, H, EpiAux{}, status, s);
+}
 
 }  // namespace
 
@@ -445,55 +541,59 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const int32_t* block_expert, const __nv_bfloat16* W1,
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
-                               cudaStream_t s, cudaEvent_t after_fc1) {
+                               cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save) {
   if (P == 0) return cudaSuccess;
   CUtensorMap mW1, mW3, mW2, mX, mH;
-  const cuuint64_t dW13[3] = {(cuuint64_t)F, (cuuint64_t)H, (cuuint64_t)E};
-  const cuuint64_t sW13[2] = {(cuuint64_t)F * 2, (cuuint64_t)H * F * 2};
-  const cuuint64_t dW2[3] = {(cuuint64_t)H, (cuuint64_t)F, (cuuint64_t)E};
-  const cuuint64_t sW2[2] = {(cuuint64_t)H * 2, (cuuint64_t)F * H * 2};
-  const cuuint32_t boxW[3] = {64, (cuuint32_t)BK, 1};
-  const cuuint64_t dX[2] = {(cuuint64_t)H, (cuuint64_t)P};
-  const cuuint64_t sX[1] = {(cuuint64_t)H * 2};
-  const cuuint64_t dH[2] = {(cuuint64_t)F, (cuuint64_t)P};
-  const cuuint64_t sH[1] = {(cuuint64_t)F * 2};
-  const cuuint32_t boxRows[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
-  if (!make_map(&mW1, W1, 3, dW13, sW13, boxW) || !make_map(&mW3, W3, 3, dW13, sW13, boxW) ||
-      !make_map(&mW2, W2, 3, dW2, sW2, boxW) || !make_map(&mX, x_perm, 2, dX, sX, boxRows) ||
-      !make_map(&mH, h, 2, dH, sH, boxRows))
+  if (!map_weights_mn(&mW1, W1, H, F, E) || !map_weights_mn(&mW3, W3, H, F, E) ||
+      !map_weights_mn(&mW2, W2, F, H, E) || !map_rows(&mX, x_perm, H, P) ||
+      !map_rows(&mH, h, F, P))
     return cudaErrorInvalidValue;
-  cudaError_t err;
+  const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
   const FfnMode mode = ffn_mode(P, E);
-  if (mode == FfnMode::kTiny) {
-    const long long nb_max = max_blocks(P, E, kBlockRowsTiny);
-    err = launch_gemm<2, true, kBlockRowsTiny, 2>(mW1, mW3, mX, offsets, block_off, num_blocks,
-                                                  block_expert, F, H, nb_max, h, F, status, s);
-    if (err != cudaSuccess) return err;
-    if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
-    return launch_gemm<1, false, kBlockRowsTiny, 2>(mW2, mW2, mH, offsets, block_off,
-                                                    num_blocks, block_expert, H, F, nb_max, y, H,
-                                                    status, s);
-  }
-  if (mode == FfnMode::kSmall) {
-    const long long nb_max = max_blocks(P, E, kBlockRows);
-    err = launch_gemm<2, true, kBlockRows, 2>(mW1, mW3, mX, offsets, block_off, num_blocks,
-                                              block_expert, F, H, nb_max, h, F, status, s);
-    if (err != cudaSuccess) return err;
-    if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
-    return launch_gemm<1, false, kBlockRows, 2>(mW2, mW2, mH, offsets, block_off, num_blocks,
-                                                block_expert, H, F, nb_max, y, H, status, s);
-  }
-  const long long nb_max = max_blocks(P, E, kBlockRowsLarge);
-  err = launch_gemm<2, true, kBlockRowsLarge, 1>(mW1, mW3, mX, offsets, block_off, num_blocks,
-                                                 block_expert, F, H, nb_max, h, F, status, s);
+  cudaError_t err;
+  if (mode == FfnMode::kTiny)
+    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
+  else if (mode == FfnMode::kSmall)
+    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
+  else
+    err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
+  if (mode == FfnMode::kTiny)
+    return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
+  if (mode == FfnMode::kSmall)
+    return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
   if (fc2_paired(H, F))
-    return launch_gemm<2, false, kBlockRowsLarge, 1>(mW2, mW2, mH, offsets, block_off,
-                                                     num_blocks, block_expert, H, F, nb_max, y,
-                                                     H, status, s);
-  return launch_gemm<1, false, kBlockRowsLarge, 2>(mW2, mW2, mH, offsets, block_off, num_blocks,
-                                                   block_expert, H, F, nb_max, y, H, status, s);
+    return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s);
+  return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
+}
+
+cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,
+                         const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                         const __nv_bfloat16* W2, const int32_t* offsets,
+                         const int32_t* block_off, const int32_t* num_blocks,
+                         const int32_t* block_expert, int P, int H, int F, int E,
+                         __nv_bfloat16* dg, __nv_bfloat16* du, __nv_bfloat16* dx_perm,
+                         int* status, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  CUtensorMap mW2k, mW1k, mW3k, mDY, mDG, mDU;
+  if (!map_weights_k(&mW2k, W2, F, H, E) || !map_weights_k(&mW1k, W1, H, F, E) ||
+      !map_weights_k(&mW3k, W3, H, F, E) || !map_rows(&mDY, dY, H, P) ||
+      !map_rows(&mDG, dg, F, P) || !map_rows(&mDU, du, F, P))
+    return cudaErrorInvalidValue;
+  const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
+  const EpiAux aux{const_cast<__nv_bfloat16*>(g), const_cast<__nv_bfloat16*>(u), dg, du, F};
+  switch (ffn_mode(P, E)) {
+    case FfnMode::kTiny:
+      return launch_dgrad_t<kBlockRowsTiny>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E,
+                                            aux, dx_perm, status, s);
+    case FfnMode::kSmall:
+      return launch_dgrad_t<kBlockRows>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E, aux,
+                                        dx_perm, status, s);
+    default:
+      return launch_dgrad_t<kBlockRowsLarge>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E,
+                                             aux, dx_perm, status, s);
+  }
 }
 
 cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T, int H,
@@ -503,27 +603,24 @@ cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, 
   if (T == 0) return cudaSuccess;
   // logits^T = Wg^T x^T: one "expert" whose weight matrix is Wg [H, E]
   CUtensorMap mG, mX;
-  const cuuint64_t dG[3] = {(cuuint64_t)E, (cuuint64_t)H, 1};
-  const cuuint64_t sG[2] = {(cuuint64_t)E * 2, (cuuint64_t)H * E * 2};
-  const cuuint32_t boxW[3] = {64, (cuuint32_t)BK, 1};
-  const cuuint64_t dX[2] = {(cuuint64_t)H, (cuuint64_t)T};
-  const cuuint64_t sX[1] = {(cuuint64_t)H * 2};
-  const cuuint32_t boxRows[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
-  if (!make_map(&mG, Wg, 3, dG, sG, boxW) || !make_map(&mX, x, 2, dX, sX, boxRows))
-    return cudaErrorInvalidValue;
-  const FfnMode mode = ffn_mode(T, 1);
-  if (mode == FfnMode::kTiny)
-    return launch_gemm<1, false, kBlockRowsTiny, 2, true>(
-        mG, mG, mX, offsets, block_off, num_blocks, block_expert, E, H,
-        max_blocks(T, 1, kBlockRowsTiny), logits, E, status, s);
-  if (mode == FfnMode::kSmall)
-    return launch_gemm<1, false, kBlockRows, 2, true>(mG, mG, mX, offsets, block_off, num_blocks,
-                                                      block_expert, E, H,
-                                                      max_blocks(T, 1, kBlockRows), logits, E,
-                                                      status, s);
-  return launch_gemm<1, false, kBlockRowsLarge, 2, true>(
-      mG, mG, mX, offsets, block_off, num_blocks, block_expert, E, H,
-      max_blocks(T, 1, kBlockRowsLarge), logits, E, status, s);
+  if (!map_weights_mn(&mG, Wg, H, E, 1) || !map_rows(&mX, x, H, T)) return cudaErrorInvalidValue;
+  const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
+  switch (ffn_mode(T, 1)) {
+    case FfnMode::kTiny:
+      return launch_gemm<1, kEpiF32, kBlockRowsTiny, 2>(mG, mG, mX, mX, pl.offsets, pl.block_off,
+                                                        pl.num_blocks, pl.block_expert, E, H,
+                                                        max_blocks(T, 1, kBlockRowsTiny), logits,
+                                                        E, EpiAux{}, status, s);
+    case FfnMode::kSmall:
+      return launch_gemm<1, kEpiF32, kBlockRows, 2>(mG, mG, mX, mX, pl.offsets, pl.block_off,
+                                                    pl.num_blocks, pl.block_expert, E, H,
+                                                    max_blocks(T, 1, kBlockRows), logits, E,
+                                                    EpiAux{}, status, s);
+    default:
+      return launch_gemm<1, kEpiF32, kBlockRowsLarge, 2>(
+          mG, mG, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, E, H,
+          max_blocks(T, 1, kBlockRowsLarge), logits, E, EpiAux{}, status, s);
+  }
 }
 
 }  // namespace moe

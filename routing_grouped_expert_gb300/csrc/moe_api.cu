@@ -92,7 +92,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                           const void* W2, int T, int H, int F, int E, int k, void* out,
                           void* ws, const WsLayout& L, cudaStream_t s,
                           const cudaEvent_t* ev = nullptr, bool clear = true,
-                          const SharedExpert* sh = nullptr) {
+                          const SharedExpert* sh = nullptr, const EpiAux* save = nullptr) {
   const int P = T * k;
   const int C = num_chunks(T, k);
   int* status = ws_ptr<int>(ws, L.status);
@@ -130,7 +130,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
-                             ev ? ev[5] : nullptr));
+                             ev ? ev[5] : nullptr, save));
   if (sh != nullptr)
     MOE_TRY(launch_grouped_ffn(static_cast<const __nv_bfloat16*>(x), sh->plan.offsets,
                                sh->plan.block_off, sh->plan.num_blocks, sh->plan.block_expert,
@@ -380,6 +380,74 @@ moe_status moe_forward_gated(const void* x, const void* Wg, const void* W1, cons
                   ws_ptr<__nv_bfloat16>(ws, G.s_y)};
   return forward_device(x, logits, W1, W3, W2, T, H, F, E, k, out, ws, L, s, nullptr,
                         /*clear=*/false, shared ? &sh : nullptr);
+}
+
+size_t moe_workspace_size_train(int T, int H, int F, int E, int k) {
+  if (!ok_sizes(T, H, F, E, k)) return 0;
+  return train_layout(T, H, F, E, k).total;
+}
+
+moe_status moe_forward_train(const void* x, const float* router_logits, const void* W1,
+                             const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                             void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  const TrainLayout R = train_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, R.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  const EpiAux save{ws_ptr<__nv_bfloat16>(ws, R.g), ws_ptr<__nv_bfloat16>(ws, R.u), nullptr,
+                    nullptr, F};
+  return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, R.base,
+                        static_cast<cudaStream_t>(stream), nullptr, true, nullptr, &save);
+}
+
+moe_status moe_backward(const void* dout, const float* router_logits, const void* W1,
+                        const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                        void* dx, float* dlogits, void* dW1, void* dW3, void* dW2, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(dout) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(dx) || !ok_ptr(dlogits) || !ok_ptr(dW1) || !ok_ptr(dW3) || !ok_ptr(dW2))
+    return MOE_ERR_INVALID_ARG;
+  const TrainLayout R = train_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, R.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout& L = R.base;
+  const int P = T * k;
+  int* status = ws_ptr<int>(ws, L.status);
+  const int32_t* topk_idx = ws_ptr<int32_t>(ws, L.topk_idx);
+  const float* topk_w = ws_ptr<float>(ws, L.topk_w);
+  const int32_t* offsets = ws_ptr<int32_t>(ws, L.offsets);
+  const int32_t* sorted_src = ws_ptr<int32_t>(ws, L.sorted_src);
+  const int32_t* dest_of = ws_ptr<int32_t>(ws, L.dest_of);
+  const __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
+  const __nv_bfloat16* h = ws_ptr<__nv_bfloat16>(ws, L.h);
+  const __nv_bfloat16* y = ws_ptr<__nv_bfloat16>(ws, L.y);
+  __nv_bfloat16* dx_perm = ws_ptr<__nv_bfloat16>(ws, R.dx_perm);
+  __nv_bfloat16* dY = ws_ptr<__nv_bfloat16>(ws, R.dY);
+  __nv_bfloat16* dg = ws_ptr<__nv_bfloat16>(ws, R.dg);
+  __nv_bfloat16* du = ws_ptr<__nv_bfloat16>(ws, R.du);
+  const auto* dout_b = static_cast<const __nv_bfloat16*>(dout);
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  MOE_TRY(launch_scale_gather(dout_b, sorted_src, topk_w, P, H, k, dY, s));
+  MOE_TRY(launch_dw_dlogits(dout_b, y, dest_of, topk_idx, router_logits, T, H, E, k, dlogits, s));
+  MOE_TRY(launch_dgrad(dY, ws_ptr<__nv_bfloat16>(ws, R.g), ws_ptr<__nv_bfloat16>(ws, R.u),
+                       static_cast<const __nv_bfloat16*>(W1),
+                       static_cast<const __nv_bfloat16*>(W3),
+                       static_cast<const __nv_bfloat16*>(W2), offsets,
+                       ws_ptr<int32_t>(ws, L.block_off), ws_ptr<int32_t>(ws, L.num_blocks),
+                       ws_ptr<int32_t>(ws, L.block_expert), P, H, F, E, dg, du, dx_perm, status,
+                       s));
+  MOE_TRY(launch_combine(dx_perm, dest_of, nullptr, T, H, k, static_cast<__nv_bfloat16*>(dx), s));
+  MOE_TRY(launch_wgrad(x_perm, h, dY, dg, du, offsets, P, H, F, E,
+                       static_cast<__nv_bfloat16*>(dW1), static_cast<__nv_bfloat16*>(dW3),
+                       static_cast<__nv_bfloat16*>(dW2), status, s));
+  return MOE_OK;
 }
 
 moe_status moe_get_device_status(const void* ws, void* stream) {

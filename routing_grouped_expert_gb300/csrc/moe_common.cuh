@@ -87,6 +87,18 @@ struct WsLayout {
   size_t total;
 };
 
+// Workspace of a training step (moe_forward_train, then moe_backward): the
+// forward layout, whose routing, x_perm, h and y_sorted the backward reads,
+// then the saved pre-activations and the backward's intermediates.
+struct TrainLayout {
+  WsLayout base;
+  size_t g, u;          // bf16[P*F]
+  size_t dY;            // bf16[P*H]
+  size_t dg, du;        // bf16[P*F]
+  size_t dx_perm;       // bf16[P*H]
+  size_t total;
+};
+
 // Workspace of the layer from hidden states (router projection + routed
 // experts + optional shared expert): the routed layout, then these regions.
 struct GatedLayout {
@@ -130,6 +142,22 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   return L;
 }
 
+inline TrainLayout train_layout(int T, int H, int F, int E, int k) {
+  TrainLayout R{};
+  R.base = ws_layout(T, H, F, E, k);
+  const size_t P = (size_t)T * k;
+  size_t o = R.base.total;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
+  R.g = take(P * F * 2);
+  R.u = take(P * F * 2);
+  R.dY = take(P * H * 2);
+  R.dg = take(P * F * 2);
+  R.du = take(P * F * 2);
+  R.dx_perm = take(P * H * 2);
+  R.total = o;
+  return R;
+}
+
 inline GatedLayout gated_layout(int T, int H, int F, int Fs, int E, int k) {
   GatedLayout G{};
   G.base = ws_layout(T, H, F, E, k);
@@ -168,12 +196,33 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32
 int ffn_block_rows(int P, int E, int H, int F);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s);
+// Extra tensors of the grouped-GEMM epilogues that read or write more than
+// their main output.
+struct EpiAux {
+  __nv_bfloat16* g;    // [rows, ld]  gate pre-activation x W1
+  __nv_bfloat16* u;    // [rows, ld]  up projection x W3
+  __nv_bfloat16* dg;   // [rows, ld]  gradients of g and u (backward)
+  __nv_bfloat16* du;
+  int ld;
+};
+// FC1 (+SwiGLU) and FC2 over the expert groups.  With `save`, FC1 also keeps
+// its pre-activations g = x W1, u = x W3 (bf16, [P, F]) for the backward.
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                const int32_t* block_off, const int32_t* num_blocks,
                                const int32_t* block_expert, const __nv_bfloat16* W1,
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
-                               cudaStream_t s, cudaEvent_t after_fc1 = nullptr);
+                               cudaStream_t s, cudaEvent_t after_fc1 = nullptr,
+                               const EpiAux* save = nullptr);
+// Backward DGrad of both expert GEMMs: dh = dY W2^T -> dg, du (SwiGLU
+// derivative from the saved g, u), dx_perm = dg W1^T + du W3^T.
+cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,
+                         const __nv_bfloat16* W1, const __nv_bfloat16* W3,
+                         const __nv_bfloat16* W2, const int32_t* offsets,
+                         const int32_t* block_off, const int32_t* num_blocks,
+                         const int32_t* block_expert, int P, int H, int F, int E,
+                         __nv_bfloat16* dg, __nv_bfloat16* du, __nv_bfloat16* dx_perm,
+                         int* status, cudaStream_t s);
 // out[t] = sum_j w[t,j] y_sorted[dest_of[t*k+j]] (+ y_shared[t] when given)
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
@@ -198,6 +247,25 @@ cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, 
 cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T, int H, int E,
                           const SingleExpertPlan& plan, float* logits, int* status,
                           cudaStream_t s);
+
+// Backward steps (training).
+cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* sorted_src,
+                                const float* topk_w, int P, int H, int k, __nv_bfloat16* dY,
+                                cudaStream_t s);
+cudaError_t launch_dw_dlogits(const __nv_bfloat16* dout, const __nv_bfloat16* y,
+                              const int32_t* dest_of, const int32_t* topk_idx,
+                              const float* logits, int T, int H, int E, int k, float* dlogits,
+                              cudaStream_t s);
+cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
+                         const __nv_bfloat16* dY, const __nv_bfloat16* dg,
+                         const __nv_bfloat16* du, const int32_t* offsets, int P, int H, int F,
+                         int E, __nv_bfloat16* dW1, __nv_bfloat16* dW3, __nv_bfloat16* dW2,
+                         int* status, cudaStream_t s);
+
+// bf16 TMA tensor map with a 128-byte swizzle; dims/strides innermost first.
+bool make_tensor_map_bf16(void* map /* CUtensorMap* */, const void* base, int rank,
+                          const unsigned long long* dims, const unsigned long long* strides,
+                          const unsigned int* box);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

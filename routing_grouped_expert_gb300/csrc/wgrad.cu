@@ -1,0 +1,346 @@
+// Backward WGrad of the expert GEMMs ("MegaFlux", §2.1: the backward streams
+// token blocks through DGrad and WGrad), per expert e over its routed rows:
+//   dW2[e] = h_e^T dY_e              (kNumB = 1: A = h, B = dY)
+//   dW1[e] = x_e^T dg_e, dW3[e] = x_e^T du_e   (kNumB = 2: A = x, B = dg, du)
+// i.e. D[m, n] = sum over the expert's rows p of A[p, m] * B[p, n].
+//
+// Tile = (expert, 128 rows m of dW, 128 columns n of dW); K = the expert's
+// rows in stages of 64.  Both operands are row-major [P, *] buffers read as
+// MN-major tensor-core operands by TMA boxes of 64 rows x 64 columns.  The
+// last stage of an expert usually runs past its rows into the next expert's:
+// before the MMAs the MMA warp zeroes those rows in shared memory (whole
+// 128-byte rows, so the swizzle does not matter), then fences them for the
+// tensor core.  Experts without rows get zero gradients.
+//
+// Warp roles as in the forward engine: warp 0 TMA producer, warp 1 MMA
+// (all lanes help zero the tail; lane 0 issues), warps 2-9 epilogue.  Every
+// wait is bounded and reports MOE_ERR_TIMEOUT.
+#include <cuda.h>
+
+#include "moe_common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = kTileM;            // dW rows per tile
+constexpr int BN = 128;               // dW columns per tile (per B operand)
+constexpr int BK = 64;                // routed rows per stage
+constexpr int kBox = 64 * BK * 2;     // one 64-column x 64-row box: 8 KB
+constexpr int kOpBytes = 2 * kBox;    // one 128-wide operand per stage: 16 KB
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSmemBudget = 204800;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+template <int kNumB>
+struct WCfg {
+  static constexpr int kStageBytes = (1 + kNumB) * kOpBytes;
+  static constexpr int kStages = kSmemBudget / kStageBytes;
+  static constexpr int kAccCols = kNumB * BN;
+  static constexpr int kTmemCols = 2 * kAccCols;   // double-buffered
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+  static_assert(kStages >= 2 && kStages <= 8, "stages");
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+};
+
+struct WBars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct WItem {
+  int e, m0, n0, row0, rows;
+};
+
+__device__ __forceinline__ WItem decode_witem(int w, int n_m, int n_n, const int32_t* offsets) {
+  WItem it;
+  const int per = n_m * n_n;
+  it.e = w / per;
+  const int r = w - it.e * per;
+  it.m0 = (r / n_n) * BM;
+  it.n0 = (r % n_n) * BN;
+  it.row0 = offsets[it.e];
+  it.rows = offsets[it.e + 1] - it.row0;
+  return it;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int kNumB>
+__global__ void __launch_bounds__(kThreads, 1)
+wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+             const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
+             int E, int M_total, int N_total, __nv_bfloat16* __restrict__ out0,
+             __nv_bfloat16* __restrict__ out1, int* __restrict__ status) {
+  using C = WCfg<kNumB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  WBars* bars = reinterpret_cast<WBars*>(smem + C::kBarOffset);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_m = M_total / BM, n_n = N_total / BN;
+  const int total = E * n_m * n_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], kEpiWarps);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (kNumB == 2) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();   // an expert's rows are re-read per tile
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const WItem it = decode_witem(w, n_m, n_n, offsets);
+        const int nkb = (it.rows + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint64_t* fb = &bars->full[stage];
+          const int r = it.row0 + kb * BK;
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(sA, &tmA, fb, it.m0, r, pol);
+          tma_load_2d(sA + kBox, &tmA, fb, it.m0 + 64, r, pol);
+#pragma unroll
+          for (int b = 0; b < kNumB; ++b) {
+            const CUtensorMap* mb = b == 0 ? &tmB0 : &tmB1;
+            uint8_t* sB = sA + (1 + b) * kOpBytes;
+            tma_load_2d(sB, mb, fb, it.n0, r, pol);
+            tma_load_2d(sB + kBox, mb, fb, it.n0 + 64, r, pol);
+          }
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailProducer);
+        *abort_flag = 1;
+      }
+      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+        mbar_wait(&bars->full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), nullptr,
+                  kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------- MMA issuer (lane 0) and tail zeroing
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t idesc = idesc_bf16(BM, BN, /*a_mn=*/true, /*b_mn=*/true);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const WItem it = decode_witem(w, n_m, n_n, offsets);
+      const int nkb = (it.rows + BK - 1) / BK;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag,
+                                             kWaitLimitNs))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs))) {
+          ok = false;
+          break;
+        }
+        const int valid = it.rows - kb * BK;     // rows of this expert in the stage
+        if (valid < BK) {
+          // zero rows [valid, 64) of every 64-row box of the stage
+          uint4* base = reinterpret_cast<uint4*>(smem + stage * C::kStageBytes);
+          const int per_box = (BK - valid) * 8;  // 16-byte chunks to clear per box
+          const int nbox = 2 * (1 + kNumB);
+          for (int i = lane; i < nbox * per_box; i += 32) {
+            const int bx = i / per_box, j = i - bx * per_box;
+            base[bx * (kBox / 16) + valid * 8 + j] = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            // both operands MN-major: 64-wide atoms 8 KB apart, 8-row groups 1 KB
+            // apart, K step of 16 rows = 2 KB
+            const uint64_t da = sdesc_sw128(a0 + kk * 2048, kBox, 1024);
+#pragma unroll
+            for (int b = 0; b < kNumB; ++b) {
+              const uint64_t db = sdesc_sw128(a0 + (1 + b) * kOpBytes + kk * 2048, kBox, 1024);
+              mma_bf16_ss(d0 + (uint32_t)(b * BN), da, db, idesc, accum);
+            }
+          }
+          mma_commit(&bars->empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bars->acc_full[acc]);   // also for an expert with no rows
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailMma);
+        *abort_flag = 1;
+      }
+      mma_commit(&bars->drain);
+      if (!mbar_wait(&bars->drain, 0, nullptr, kWaitLimitNs))
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailDrain);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+      const WItem it = decode_witem(w, n_m, n_n, offsets);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[acc], acc_phase, abort_flag,
+                                             kWaitLimitNs))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int m = it.m0 + q * 32 + lane;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+#pragma unroll
+      for (int b = 0; b < kNumB; ++b) {
+        __nv_bfloat16* row = (b == 0 ? out0 : out1) +
+                             ((size_t)it.e * M_total + m) * N_total + it.n0;
+        for (int c0 = 16 * half; c0 < BN; c0 += 32) {
+          uint32_t v[16];
+          if (it.rows > 0) {
+            tmem_ld_32x32b_x16(tb + b * BN + c0, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = 0u;
+          }
+          uint4 packed[2];
+          __nv_bfloat162* pk = reinterpret_cast<__nv_bfloat162*>(packed);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            pk[c] = __floats2bfloat162_rn(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+          reinterpret_cast<uint4*>(row + c0)[0] = packed[0];
+          reinterpret_cast<uint4*>(row + c0)[1] = packed[1];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// Row-major [P, cols] buffer as MN-major operand boxes of 64 columns x 64 rows.
+bool map_rows64(CUtensorMap* m, const void* X, int cols, int P) {
+  const cuuint64_t d[2] = {(cuuint64_t)cols, (cuuint64_t)P};
+  const cuuint64_t st[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)BK};
+  return make_tensor_map_bf16(m, X, 2, reinterpret_cast<const unsigned long long*>(d),
+                              reinterpret_cast<const unsigned long long*>(st),
+                              reinterpret_cast<const unsigned int*>(box));
+}
+
+template <int kNumB>
+cudaError_t launch_w(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                     const int32_t* offsets, int E, int M_total, int N_total, __nv_bfloat16* o0,
+                     __nv_bfloat16* o1, int* status, cudaStream_t s) {
+  using C = WCfg<kNumB>;
+  cudaError_t err = cudaFuncSetAttribute(wgrad_kernel<kNumB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const long long items = (long long)E * (M_total / BM) * (N_total / BN);
+  const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
+  wgrad_kernel<kNumB><<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, offsets, E, M_total,
+                                                            N_total, o0, o1, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
+                         const __nv_bfloat16* dY, const __nv_bfloat16* dg,
+                         const __nv_bfloat16* du, const int32_t* offsets, int P, int H, int F,
+                         int E, __nv_bfloat16* dW1, __nv_bfloat16* dW3, __nv_bfloat16* dW2,
+                         int* status, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  CUtensorMap mX, mH, mDY, mDG, mDU;
+  if (!map_rows64(&mX, x_perm, H, P) || !map_rows64(&mH, h, F, P) ||
+      !map_rows64(&mDY, dY, H, P) || !map_rows64(&mDG, dg, F, P) || !map_rows64(&mDU, du, F, P))
+    return cudaErrorInvalidValue;
+  cudaError_t err = launch_w<1>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s);
+  if (err != cudaSuccess) return err;
+  return launch_w<2>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s);
+}
+
+}  // namespace moe

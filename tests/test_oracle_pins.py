@@ -342,6 +342,15 @@ def test_backward_finite_differences():
         assert abs(fd - g[key][pos]) <= tol * max(1.0, abs(fd)), (name, fd, g[key][pos])
 
 
+def test_backward_magnitudes_bound_the_gradients():
+    x, logits, W1, W3, W2 = rand_layer(30, 8, 12, 4, 2, seed=25)
+    dout = np.random.default_rng(26).standard_normal((30, 8))
+    g = O.backward(x, logits, W1, W3, W2, 2, dout, magnitudes=True)
+    for n in ("dx", "dlogits", "dW1", "dW3", "dW2"):
+        assert np.all(g["mag_" + n] >= np.abs(g[n]) - 1e-12), n   # triangle inequality
+        assert np.all(g["mag_" + n] >= 0)
+
+
 def test_backward_top1_has_no_logit_gradient():
     x, logits, W1, W3, W2 = rand_layer(20, 8, 12, 4, 1, seed=23)
     dout = np.random.default_rng(24).standard_normal((20, 8))
