@@ -53,6 +53,8 @@ def parse():
                     help="T,H,F,E,k: a uniform-routing workload of these sizes instead")
     ap.add_argument("--sweep", action="store_true",
                     help="tokens-per-expert sweep of the workload's shape (own JSON line)")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step: moe_forward_train + moe_backward (own JSON line)")
     ap.add_argument("--gated", action="store_true",
                     help="time the layer from hidden states (router projection + routed "
                          "experts + --shared-f shared expert) instead (own JSON line)")
@@ -569,8 +571,58 @@ def bench_gated(args):
                                "peak_source": peak_src}}
 
 
+# --------------------------------------------------------- training step
+def bench_train(args):
+    """moe_forward_train then moe_backward on the workload, dout ~ N(0, 1).
+    FLOPs: forward 2*T*k*3*H*F, backward twice that (DGrad and WGrad)."""
+    import routing_grouped_expert_gb300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[args.workload]
+    d = I.make_inputs(wl, dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    dout = torch.randn(wl.T, wl.H, generator=g, device=dev).to(torch.bfloat16)
+    ws = moe.Workspace(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        moe.moe_forward_train(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k, ws)
+        if ev:
+            ev[1].record()
+        r = moe.moe_backward(dout, d["logits"], d["W1"], d["W3"], d["W2"], wl.k, ws)
+        if ev:
+            ev[2].record()
+        return r
+    for _ in range(args.warmup):
+        step()
+    if moe.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    fwd = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    ms = fwd + bwd
+    peaks, peak_src = load_peaks()
+    f_flops = acc.ffn_flops(wl.T, wl.H, wl.F, wl.k)
+    flops = 3 * f_flops
+    return {"metric": METRIC, "mode": "train", "value": round(wl.T / (ms / 1e3), 1), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "forward_ms": round(fwd, 4), "backward_ms": round(bwd, 4),
+            "steps": args.steps, "config": wl_config(wl, {"dout": "N(0,1) bf16"}),
+            "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+            "backward_tflops": round(2 * f_flops / (bwd / 1e3) / 1e12, 1),
+            "frac_of_bf16_peak": round(flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+            "peak_source": peak_src}
+
+
 def main():
     args = parse()
+    if args.train:
+        print(json.dumps(bench_train(args)), flush=True)
+        return
     if args.gated:
         print(json.dumps(bench_gated(args)), flush=True)
         return
