@@ -61,7 +61,8 @@ enum : int {
 };
 
 // kNumA weight tiles of 128 rows share each token block (FC1: gate and up of
-// the same features; FC2 with kNumA = 2: two adjacent feature tiles).
+// the same features; otherwise, with kNumA = 2: two adjacent feature tiles,
+// which halves the token-block bytes staged per MMA).
 // kBN = token rows per block, kAccBufs = TMEM accumulator buffers.
 // kAKMajor: the weight tile is read K-major (the backward's W^T products)
 // instead of MN-major.  kDualK: the K loop runs twice, first over
@@ -81,8 +82,8 @@ struct Cfg {
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
-  static_assert((kEpi != kEpiF32 && kEpi != kEpiSwigluBwd) || kNumA == 1, "single tile");
-  static_assert(!kDualK || (kNumA == 1 && kAKMajor), "two-phase K: one K-major tile");
+  static_assert(kEpi != kEpiF32 || kNumA == 1, "single tile");
+  static_assert(!kDualK || kAKMajor, "two-phase K: K-major weight tiles");
 };
 
 struct Bars {
@@ -346,12 +347,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
               aux.u[row * aux.ld + feat] = __float2bfloat16_rn(a1);
             }
           } else if constexpr (kEpi == kEpiSwigluBwd) {
-            const float gv = __bfloat162float(aux.g[row * aux.ld + feat]);
-            const float uv = __bfloat162float(aux.u[row * aux.ld + feat]);
-            const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
-            aux.dg[row * aux.ld + feat] =
-                __float2bfloat16_rn(a0 * uv * sg * (1.0f + gv * (1.0f - sg)));
-            aux.du[row * aux.ld + feat] = __float2bfloat16_rn(a0 * gv * sg);
+#pragma unroll
+            for (int a = 0; a < kNumA; ++a) {
+              const float dh = a == 0 ? a0 : __uint_as_float(g2[c]);
+              const size_t i = row * aux.ld + feat + a * BM;
+              const float gv = __bfloat162float(aux.g[i]);
+              const float uv = __bfloat162float(aux.u[i]);
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+              aux.dg[i] = __float2bfloat16_rn(dh * uv * sg * (1.0f + gv * (1.0f - sg)));
+              aux.du[i] = __float2bfloat16_rn(dh * gv * sg);
+            }
           } else {
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out_ptr) + row * ld_out + feat;
             o[0] = __float2bfloat16_rn(a0);
@@ -506,20 +511,25 @@ cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const Plan
                                                   s);
 }
 
-template <int kBN>
+// kPairF / kPairH: pair adjacent weight tiles (single-buffered accumulators)
+// in the dh / dx products; worth it for large blocks, whose long K keeps the
+// unoverlapped epilogue a small share of a tile.
+template <int kBN, bool kPairF, bool kPairH>
 cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
                            const CUtensorMap& mW1k, const CUtensorMap& mW3k,
                            const CUtensorMap& mDG, const CUtensorMap& mDU, const PlanPtrs& pl,
                            int P, int H, int F, int E, const EpiAux& aux,
                            __nv_bfloat16* dx_perm, int* status, cudaStream_t s) {
   const long long nb_max = max_blocks(P, E, kBN);
+  constexpr int kAF = kPairF ? 2 : 1, kBufF = kPairF ? 1 : 2;
+  constexpr int kAH = kPairH ? 2 : 1, kBufH = kPairH ? 1 : 2;
   // dh = dY W2[e]^T (M = F, K = H), then the SwiGLU derivative -> dg, du
-  cudaError_t err = launch_gemm<1, kEpiSwigluBwd, kBN, 2, true>(
+  cudaError_t err = launch_gemm<kAF, kEpiSwigluBwd, kBN, kBufF, true>(
       mW2k, mW2k, mDY, mDY, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H,
       nb_max, nullptr, 0, aux, status, s);
   if (err != cudaSuccess) return err;
   // dx_perm = dg W1[e]^T + du W3[e]^T (M = H, K = F in two phases)
-  return launch_gemm<1, kEpiBf16, kBN, 2, true, true>(
+  return launch_gemm<kAH, kEpiBf16, kBN, kBufH, true, true>(
       mW1k, mW3k, mDG, mDU, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
       nb_max, dx_perm, H, EpiAux{}, status, s);
 }
@@ -585,14 +595,25 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
   const EpiAux aux{const_cast<__nv_bfloat16*>(g), const_cast<__nv_bfloat16*>(u), dg, du, F};
   switch (ffn_mode(P, E)) {
     case FfnMode::kTiny:
-      return launch_dgrad_t<kBlockRowsTiny>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E,
-                                            aux, dx_perm, status, s);
+      return launch_dgrad_t<kBlockRowsTiny, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P,
+                                                          H, F, E, aux, dx_perm, status, s);
     case FfnMode::kSmall:
-      return launch_dgrad_t<kBlockRows>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E, aux,
-                                        dx_perm, status, s);
-    default:
-      return launch_dgrad_t<kBlockRowsLarge>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H, F, E,
-                                             aux, dx_perm, status, s);
+      return launch_dgrad_t<kBlockRows, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H,
+                                                      F, E, aux, dx_perm, status, s);
+    default: {
+      const bool pf = F % (2 * BM) == 0, ph = H % (2 * BM) == 0;
+      if (pf && ph)
+        return launch_dgrad_t<kBlockRowsLarge, true, true>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
+                                                           P, H, F, E, aux, dx_perm, status, s);
+      if (pf)
+        return launch_dgrad_t<kBlockRowsLarge, true, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
+                                                            P, H, F, E, aux, dx_perm, status, s);
+      if (ph)
+        return launch_dgrad_t<kBlockRowsLarge, false, true>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
+                                                            P, H, F, E, aux, dx_perm, status, s);
+      return launch_dgrad_t<kBlockRowsLarge, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
+                                                           P, H, F, E, aux, dx_perm, status, s);
+    }
   }
 }
 

@@ -26,7 +26,10 @@ EPS = 2.0 ** -9
 CASES = {  # name: (T, H, F, E, k) -- block mode from the mean rows per expert
     "tiny_blocks": (64, 256, 384, 8, 2),
     "small_blocks": (200, 384, 512, 6, 3),
-    "large_blocks_ragged": (300, 256, 256, 4, 2),
+    "large_blocks_ragged": (300, 256, 256, 4, 2),      # paired dh and dx tiles
+    "large_unpaired": (400, 384, 384, 4, 2),           # H, F not multiples of 256
+    "large_pair_f_only": (400, 384, 512, 4, 2),
+    "large_multi_block": (600, 256, 512, 2, 2),        # three blocks per expert
     "many_empty_experts": (20, 128, 256, 32, 1),
     "fine_grained_like": (150, 256, 128, 32, 6),
 }
