@@ -327,6 +327,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
         uint32_t g[16], g2[16];
+        float pg[kNumA][16], pu[kNumA][16];
+        if constexpr (kEpi == kEpiSwigluBwd) {
+          // all saved g, u of the chunk are loaded first: a load placed after a
+          // store to dg / du would otherwise wait for it (possible aliasing)
+#pragma unroll
+          for (int a = 0; a < kNumA; ++a)
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const bool in = c0 + c < it.nrows;
+              const size_t i = (size_t)(it.row0 + c0 + c) * aux.ld + feat + a * BM;
+              pg[a][c] = in ? __bfloat162float(aux.g[i]) : 0.f;
+              pu[a][c] = in ? __bfloat162float(aux.u[i]) : 0.f;
+            }
+        }
         tmem_ld_32x32b_x16(tb + c0, g);
         if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
         tmem_ld_wait();
@@ -351,8 +365,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             for (int a = 0; a < kNumA; ++a) {
               const float dh = a == 0 ? a0 : __uint_as_float(g2[c]);
               const size_t i = row * aux.ld + feat + a * BM;
-              const float gv = __bfloat162float(aux.g[i]);
-              const float uv = __bfloat162float(aux.u[i]);
+              const float gv = pg[a][c], uv = pu[a][c];
               const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
               aux.dg[i] = __float2bfloat16_rn(dh * uv * sg * (1.0f + gv * (1.0f - sg)));
               aux.du[i] = __float2bfloat16_rn(dh * gv * sg);

@@ -4,9 +4,14 @@
 //   dW1[e] = x_e^T dg_e, dW3[e] = x_e^T du_e   (kNumB = 2: A = x, B = dg, du)
 // i.e. D[m, n] = sum over the expert's rows p of A[p, m] * B[p, n].
 //
-// Tile = (expert, 128 rows m of dW, 128 columns n of dW); K = the expert's
-// rows in stages of 64.  Both operands are row-major [P, *] buffers read as
-// MN-major tensor-core operands by TMA boxes of 64 rows x 64 columns.  The
+// Tile = (expert, rows m of dW, columns n of dW); K = the expert's rows in
+// stages of 64.  Two tile shapes: 128 x 128 per B operand with two TMEM
+// accumulator buffers (the epilogue of one tile overlaps the MMAs of the
+// next), or, with kPairM, 256 x 256 (two 128-row A sub-tiles sharing the B
+// columns) in one buffer, which halves the operand bytes staged per MMA and
+// so keeps the tensor core fed when an expert has many rows.  Both operands
+// are row-major [P, *] buffers read as MN-major tensor-core operands by TMA
+// boxes of 64 rows x 64 columns.  The
 // last stage of an expert usually runs past its rows into the next expert's:
 // before the MMAs the MMA warp zeroes those rows in shared memory (whole
 // 128-byte rows, so the swizzle does not matter), then fences them for the
@@ -25,22 +30,26 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = kTileM;            // dW rows per tile
-constexpr int BN = 128;               // dW columns per tile (per B operand)
+constexpr int BM = kTileM;            // dW rows per MMA
 constexpr int BK = 64;                // routed rows per stage
 constexpr int kBox = 64 * BK * 2;     // one 64-column x 64-row box: 8 KB
-constexpr int kOpBytes = 2 * kBox;    // one 128-wide operand per stage: 16 KB
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 204800;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-template <int kNumB>
+template <int kNumB, bool kPairM>
 struct WCfg {
-  static constexpr int kStageBytes = (1 + kNumB) * kOpBytes;
+  static constexpr int kMS = kPairM ? 2 : 1;                      // 128-row A sub-tiles
+  static constexpr int kBN = (kPairM && kNumB == 1) ? 256 : 128;  // columns per B operand
+  static constexpr int kTileRows = kMS * BM;
+  static constexpr int kABytes = kMS * 2 * kBox;
+  static constexpr int kBBytes = (kBN / 64) * kBox;
+  static constexpr int kStageBytes = kABytes + kNumB * kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
-  static constexpr int kAccCols = kNumB * BN;
-  static constexpr int kTmemCols = 2 * kAccCols;   // double-buffered
+  static constexpr int kAccCols = kMS * kNumB * kBN;
+  static constexpr int kAccBufs = kPairM ? 1 : 2;
+  static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
   static_assert(kStages >= 2 && kStages <= 8, "stages");
@@ -61,13 +70,14 @@ struct WItem {
   int e, m0, n0, row0, rows;
 };
 
+template <int kTileRows, int kBN>
 __device__ __forceinline__ WItem decode_witem(int w, int n_m, int n_n, const int32_t* offsets) {
   WItem it;
   const int per = n_m * n_n;
   it.e = w / per;
   const int r = w - it.e * per;
-  it.m0 = (r / n_n) * BM;
-  it.n0 = (r % n_n) * BN;
+  it.m0 = (r / n_n) * kTileRows;
+  it.n0 = (r % n_n) * kBN;
   it.row0 = offsets[it.e];
   it.rows = offsets[it.e + 1] - it.row0;
   return it;
@@ -77,19 +87,20 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int kNumB>
+template <int kNumB, bool kPairM>
 __global__ void __launch_bounds__(kThreads, 1)
 wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
              const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
              int E, int M_total, int N_total, __nv_bfloat16* __restrict__ out0,
              __nv_bfloat16* __restrict__ out1, int* __restrict__ status) {
-  using C = WCfg<kNumB>;
+  using C = WCfg<kNumB, kPairM>;
+  constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   WBars* bars = reinterpret_cast<WBars*>(smem + C::kBarOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_m = M_total / BM, n_n = N_total / BN;
+  const int n_m = M_total / C::kTileRows, n_n = N_total / kBN;
   const int total = E * n_m * n_n;
 
   if (threadIdx.x == 0) {
@@ -97,7 +108,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&bars->acc_full[b], 1);
       mbar_init(&bars->acc_empty[b], kEpiWarps);
     }
@@ -128,7 +139,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       uint32_t phase = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const WItem it = decode_witem(w, n_m, n_n, offsets);
+        const WItem it = decode_witem<C::kTileRows, kBN>(w, n_m, n_n, offsets);
         const int nkb = (it.rows + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -139,14 +150,16 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           uint64_t* fb = &bars->full[stage];
           const int r = it.row0 + kb * BK;
           mbar_arrive_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(sA, &tmA, fb, it.m0, r, pol);
-          tma_load_2d(sA + kBox, &tmA, fb, it.m0 + 64, r, pol);
+#pragma unroll
+          for (int bx = 0; bx < 2 * C::kMS; ++bx)
+            tma_load_2d(sA + bx * kBox, &tmA, fb, it.m0 + 64 * bx, r, pol);
 #pragma unroll
           for (int b = 0; b < kNumB; ++b) {
             const CUtensorMap* mb = b == 0 ? &tmB0 : &tmB1;
-            uint8_t* sB = sA + (1 + b) * kOpBytes;
-            tma_load_2d(sB, mb, fb, it.n0, r, pol);
-            tma_load_2d(sB + kBox, mb, fb, it.n0 + 64, r, pol);
+            uint8_t* sB = sA + C::kABytes + b * C::kBBytes;
+#pragma unroll
+            for (int bx = 0; bx < kBN / 64; ++bx)
+              tma_load_2d(sB + bx * kBox, mb, fb, it.n0 + 64 * bx, r, pol);
           }
           ++issued;
           if (++stage == C::kStages) {
@@ -166,12 +179,12 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   } else if (warp == 1) {
     // ---------------------------------- MMA issuer (lane 0) and tail zeroing
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t idesc = idesc_bf16(BM, BN, /*a_mn=*/true, /*b_mn=*/true);
+    const uint32_t idesc = idesc_bf16(BM, kBN, /*a_mn=*/true, /*b_mn=*/true);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const WItem it = decode_witem(w, n_m, n_n, offsets);
+      const WItem it = decode_witem<C::kTileRows, kBN>(w, n_m, n_n, offsets);
       const int nkb = (it.rows + BK - 1) / BK;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag,
                                              kWaitLimitNs))) {
@@ -191,7 +204,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           // zero rows [valid, 64) of every 64-row box of the stage
           uint4* base = reinterpret_cast<uint4*>(smem + stage * C::kStageBytes);
           const int per_box = (BK - valid) * 8;  // 16-byte chunks to clear per box
-          const int nbox = 2 * (1 + kNumB);
+          const int nbox = C::kStageBytes / kBox;
           for (int i = lane; i < nbox * per_box; i += 32) {
             const int bx = i / per_box, j = i - bx * per_box;
             base[bx * (kBox / 16) + valid * 8 + j] = make_uint4(0, 0, 0, 0);
@@ -207,11 +220,15 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             // both operands MN-major: 64-wide atoms 8 KB apart, 8-row groups 1 KB
             // apart, K step of 16 rows = 2 KB
-            const uint64_t da = sdesc_sw128(a0 + kk * 2048, kBox, 1024);
 #pragma unroll
-            for (int b = 0; b < kNumB; ++b) {
-              const uint64_t db = sdesc_sw128(a0 + (1 + b) * kOpBytes + kk * 2048, kBox, 1024);
-              mma_bf16_ss(d0 + (uint32_t)(b * BN), da, db, idesc, accum);
+            for (int ms = 0; ms < C::kMS; ++ms) {
+              const uint64_t da = sdesc_sw128(a0 + ms * 2 * kBox + kk * 2048, kBox, 1024);
+#pragma unroll
+              for (int b = 0; b < kNumB; ++b) {
+                const uint64_t db =
+                    sdesc_sw128(a0 + C::kABytes + b * C::kBBytes + kk * 2048, kBox, 1024);
+                mma_bf16_ss(d0 + (uint32_t)((ms * kNumB + b) * kBN), da, db, idesc, accum);
+              }
             }
           }
           mma_commit(&bars->empty[stage]);
@@ -225,7 +242,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       if (!ok) break;
       if (lane == 0) mma_commit(&bars->acc_full[acc]);   // also for an expert with no rows
       __syncwarp();
-      if (++acc == 2) {
+      if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -247,23 +264,24 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      const WItem it = decode_witem(w, n_m, n_n, offsets);
+      const WItem it = decode_witem<C::kTileRows, kBN>(w, n_m, n_n, offsets);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[acc], acc_phase, abort_flag,
                                              kWaitLimitNs))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int m = it.m0 + q * 32 + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
 #pragma unroll
-      for (int b = 0; b < kNumB; ++b) {
+      for (int t = 0; t < C::kMS * kNumB; ++t) {
+        const int ms = t / kNumB, b = t % kNumB;
+        const int m = it.m0 + ms * BM + q * 32 + lane;
         __nv_bfloat16* row = (b == 0 ? out0 : out1) +
                              ((size_t)it.e * M_total + m) * N_total + it.n0;
-        for (int c0 = 16 * half; c0 < BN; c0 += 32) {
+        for (int c0 = 16 * half; c0 < kBN; c0 += 32) {
           uint32_t v[16];
           if (it.rows > 0) {
-            tmem_ld_32x32b_x16(tb + b * BN + c0, v);
+            tmem_ld_32x32b_x16(tb + t * kBN + c0, v);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -281,7 +299,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
-      if (++acc == 2) {
+      if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -310,21 +328,27 @@ bool map_rows64(CUtensorMap* m, const void* X, int cols, int P) {
                               reinterpret_cast<const unsigned int*>(box));
 }
 
-template <int kNumB>
+template <int kNumB, bool kPairM>
 cudaError_t launch_w(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                      const int32_t* offsets, int E, int M_total, int N_total, __nv_bfloat16* o0,
                      __nv_bfloat16* o1, int* status, cudaStream_t s) {
-  using C = WCfg<kNumB>;
-  cudaError_t err = cudaFuncSetAttribute(wgrad_kernel<kNumB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  using C = WCfg<kNumB, kPairM>;
+  auto kern = wgrad_kernel<kNumB, kPairM>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const long long items = (long long)E * (M_total / BM) * (N_total / BN);
+  const long long items = (long long)E * (M_total / C::kTileRows) * (N_total / C::kBN);
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  wgrad_kernel<kNumB><<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, offsets, E, M_total,
-                                                            N_total, o0, o1, status);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, offsets, E, M_total, N_total, o0, o1,
+                                             status);
   return cudaGetLastError();
 }
+
+// 256 x 256 tiles once an expert has, on average, this many rows: enough K
+// per tile that the unoverlapped epilogue is a small share of it.
+#ifndef MOE_WGRAD_PAIR_MIN_ROWS
+#define MOE_WGRAD_PAIR_MIN_ROWS 512
+#endif
 
 }  // namespace
 
@@ -338,9 +362,14 @@ cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
   if (!map_rows64(&mX, x_perm, H, P) || !map_rows64(&mH, h, F, P) ||
       !map_rows64(&mDY, dY, H, P) || !map_rows64(&mDG, dg, F, P) || !map_rows64(&mDU, du, F, P))
     return cudaErrorInvalidValue;
-  cudaError_t err = launch_w<1>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s);
+  const bool deep = (long long)P >= (long long)MOE_WGRAD_PAIR_MIN_ROWS * E;
+  const bool pair = deep && H % 256 == 0 && F % 256 == 0;
+  cudaError_t err = pair ? launch_w<1, true>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s)
+                         : launch_w<1, false>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s);
   if (err != cudaSuccess) return err;
-  return launch_w<2>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s);
+  return (deep && H % 256 == 0)
+             ? launch_w<2, true>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s)
+             : launch_w<2, false>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s);
 }
 
 }  // namespace moe

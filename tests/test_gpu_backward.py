@@ -29,7 +29,8 @@ CASES = {  # name: (T, H, F, E, k) -- block mode from the mean rows per expert
     "large_blocks_ragged": (300, 256, 256, 4, 2),      # paired dh and dx tiles
     "large_unpaired": (400, 384, 384, 4, 2),           # H, F not multiples of 256
     "large_pair_f_only": (400, 384, 512, 4, 2),
-    "large_multi_block": (600, 256, 512, 2, 2),        # three blocks per expert
+    "large_multi_block": (600, 256, 512, 2, 2),        # three blocks; 256 x 256 WGrad
+    "deep_wgrad_f384": (600, 256, 384, 2, 2),          # dW2 128-wide, dW1/dW3 256 x 256
     "many_empty_experts": (20, 128, 256, 32, 1),
     "fine_grained_like": (150, 256, 128, 32, 6),
 }
