@@ -18,8 +18,12 @@
 // tensor core.  Experts without rows get zero gradients.
 //
 // Warp roles as in the forward engine: warp 0 TMA producer, warp 1 MMA
-// (all lanes help zero the tail; lane 0 issues), warps 2-9 epilogue.  Every
-// wait is bounded and reports MOE_ERR_TIMEOUT.
+// (all lanes help zero the tail; lane 0 issues), warps 2-9 epilogue.  The
+// epilogue converts 32 rows x 64 columns at a time to bf16 in a 128-byte-
+// swizzled staging buffer of its own (4 KB per warp) and writes it with a
+// TMA store, so the gradient leaves in whole lines without holding the warp;
+// the accumulator buffer is released as soon as its last columns are read.
+// Every wait is bounded and reports MOE_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "moe_common.cuh"
@@ -35,7 +39,8 @@ constexpr int BK = 64;                // routed rows per stage
 constexpr int kBox = 64 * BK * 2;     // one 64-column x 64-row box: 8 KB
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kSmemBudget = 204800;
+constexpr int kSmemBudget = 196608;   // operand ring
+constexpr int kStgBytes = 32 * 64 * 2; // epilogue staging per warp: 32 rows x 64 columns
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 template <int kNumB, bool kPairM>
@@ -51,7 +56,9 @@ struct WCfg {
   static constexpr int kAccBufs = kPairM ? 1 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+  static constexpr int kStgOffset = kBarOffset + 1024;              // 1 KB-aligned for the swizzle
+  static constexpr int kSmemBytes = kStgOffset + kEpiWarps * kStgBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
 };
@@ -90,9 +97,9 @@ __device__ __forceinline__ void fence_async_smem() {
 template <int kNumB, bool kPairM>
 __global__ void __launch_bounds__(kThreads, 1)
 wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-             const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
-             int E, int M_total, int N_total, __nv_bfloat16* __restrict__ out0,
-             __nv_bfloat16* __restrict__ out1, int* __restrict__ status) {
+             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+             const __grid_constant__ CUtensorMap tmO1, const int32_t* __restrict__ offsets,
+             int E, int M_total, int N_total, int* __restrict__ status) {
   using C = WCfg<kNumB, kPairM>;
   constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
@@ -258,8 +265,10 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int q = warp & 3;            // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;  // which alternate 64-column chunks it takes
+    uint8_t* stg = smem + C::kStgOffset + (warp - 2) * kStgBytes;
+    constexpr int kChunks = C::kMS * kNumB * (kBN / 128);   // per warp per tile
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -272,41 +281,61 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      int chunk = 0;
 #pragma unroll
       for (int t = 0; t < C::kMS * kNumB; ++t) {
         const int ms = t / kNumB, b = t % kNumB;
-        const int m = it.m0 + ms * BM + q * 32 + lane;
-        __nv_bfloat16* row = (b == 0 ? out0 : out1) +
-                             ((size_t)it.e * M_total + m) * N_total + it.n0;
-        for (int c0 = 16 * half; c0 < kBN; c0 += 32) {
-          uint32_t v[16];
+        const int orow = it.e * M_total + it.m0 + ms * BM + q * 32;   // the warp's first row
+#pragma unroll
+        for (int c0 = 64 * half; c0 < kBN; c0 += 128, ++chunk) {
+          uint32_t v[64];
           if (it.rows > 0) {
-            tmem_ld_32x32b_x16(tb + t * kBN + c0, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tmem_ld_32x32b_x16(tb + t * kBN + c0 + 16 * i,
+                                 *reinterpret_cast<uint32_t(*)[16]>(&v[16 * i]));
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = 0u;
+            for (int c = 0; c < 64; ++c) v[c] = 0u;
           }
-          uint4 packed[2];
-          __nv_bfloat162* pk = reinterpret_cast<__nv_bfloat162*>(packed);
+          if (chunk == kChunks - 1) {   // accumulator read out: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+          }
+          if (lane == 0) bulk_wait_read_all();   // the previous store has left the buffer
+          __syncwarp();
+          // row `lane` of the box: 16-byte chunk j sits at j ^ (row & 7) (128B swizzle)
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            pk[c] = __floats2bfloat162_rn(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
-          reinterpret_cast<uint4*>(row + c0)[0] = packed[0];
-          reinterpret_cast<uint4*>(row + c0)[1] = packed[1];
+          for (int j = 0; j < 8; ++j) {
+            uint4 pk;
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              p2[c] = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * c]),
+                                            __uint_as_float(v[8 * j + 2 * c + 1]));
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(b == 0 ? &tmO0 : &tmO1, stg, it.n0 + c0, orow);
+            bulk_commit();
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
       if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
-    if (!ok && lane == 0) {
-      set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
-      *abort_flag = 1;
+    if (lane == 0) {
+      bulk_wait_all();   // every gradient tile written before the CTA leaves
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
+        *abort_flag = 1;
+      }
     }
   }
 
@@ -328,18 +357,32 @@ bool map_rows64(CUtensorMap* m, const void* X, int cols, int P) {
                               reinterpret_cast<const unsigned int*>(box));
 }
 
+// Gradient [E, M, N] (N contiguous) as 2-D [E * M, N] store boxes of 32 rows
+// x 64 columns.
+bool map_grad_out(CUtensorMap* m, const void* W, int E, int M, int N) {
+  const cuuint64_t d[2] = {(cuuint64_t)N, (cuuint64_t)E * M};
+  const cuuint64_t st[1] = {(cuuint64_t)N * 2};
+  const cuuint32_t box[2] = {64, 32};
+  return make_tensor_map_bf16(m, W, 2, reinterpret_cast<const unsigned long long*>(d),
+                              reinterpret_cast<const unsigned long long*>(st),
+                              reinterpret_cast<const unsigned int*>(box));
+}
+
 template <int kNumB, bool kPairM>
 cudaError_t launch_w(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                      const int32_t* offsets, int E, int M_total, int N_total, __nv_bfloat16* o0,
                      __nv_bfloat16* o1, int* status, cudaStream_t s) {
   using C = WCfg<kNumB, kPairM>;
+  CUtensorMap mo0, mo1;
+  if (!map_grad_out(&mo0, o0, E, M_total, N_total) || !map_grad_out(&mo1, o1, E, M_total, N_total))
+    return cudaErrorInvalidValue;
   auto kern = wgrad_kernel<kNumB, kPairM>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long items = (long long)E * (M_total / C::kTileRows) * (N_total / C::kBN);
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, offsets, E, M_total, N_total, o0, o1,
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, mo0, mo1, offsets, E, M_total, N_total,
                                              status);
   return cudaGetLastError();
 }
