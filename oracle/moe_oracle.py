@@ -313,15 +313,15 @@ def backward(x, logits, W1, W3, W2, k: int, dout, magnitudes: bool = False):
     mdx = np.zeros((T, H))
     mdw = np.zeros((T, k))
     for e in range(E):
-        W1e, W3e, W2e = _f64(W1[e]), _f64(W3[e]), _f64(W2[e])
         lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if lo == hi:
+            for name, like in (("dW1", W1[e]), ("dW3", W3[e]), ("dW2", W2[e])):
+                grads[name].append(np.zeros(tuple(like.shape)))
+                mag[name].append(np.zeros(tuple(like.shape)))
+            continue
+        W1e, W3e, W2e = _f64(W1[e]), _f64(W3[e]), _f64(W2[e])
         a = sorted_src[lo:hi]
         t, j = a // k, a % k
-        if lo == hi:
-            for name, like in (("dW1", W1e), ("dW3", W3e), ("dW2", W2e)):
-                grads[name].append(np.zeros_like(like))
-                mag[name].append(np.zeros_like(like))
-            continue
         X = x64[t]
         g, u = _mm(X, W1e), _mm(X, W3e)
         s = 1.0 / (1.0 + np.exp(-g))

@@ -5,11 +5,12 @@
 // i.e. D[m, n] = sum over the expert's rows p of A[p, m] * B[p, n].
 //
 // Tile = (expert, rows m of dW, columns n of dW); K = the expert's rows in
-// stages of 64.  Two tile shapes: 128 x 128 per B operand with two TMEM
-// accumulator buffers (the epilogue of one tile overlaps the MMAs of the
-// next), or, with kPairM, 256 x 256 (two 128-row A sub-tiles sharing the B
-// columns) in one buffer, which halves the operand bytes staged per MMA and
-// so keeps the tensor core fed when an expert has many rows.  Both operands
+// stages of 64.  Two tile shapes: with kPairM (used whenever the sizes are
+// multiples of 256), 256 x 256 (two 128-row A sub-tiles sharing the B
+// columns) in one TMEM buffer, which halves the operand bytes staged per MMA
+// and so keeps the tensor core fed; otherwise 128 x 128 per B operand with
+// two accumulator buffers (the epilogue of one tile overlaps the MMAs of the
+// next).  Both operands
 // are row-major [P, *] buffers read as MN-major tensor-core operands by TMA
 // boxes of 64 rows x 64 columns.  The
 // last stage of an expert usually runs past its rows into the next expert's:
@@ -387,11 +388,6 @@ cudaError_t launch_w(const CUtensorMap& a, const CUtensorMap& b0, const CUtensor
   return cudaGetLastError();
 }
 
-// 256 x 256 tiles once an expert has, on average, this many rows: enough K
-// per tile that the unoverlapped epilogue is a small share of it.
-#ifndef MOE_WGRAD_PAIR_MIN_ROWS
-#define MOE_WGRAD_PAIR_MIN_ROWS 512
-#endif
 
 }  // namespace
 
@@ -405,12 +401,14 @@ cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
   if (!map_rows64(&mX, x_perm, H, P) || !map_rows64(&mH, h, F, P) ||
       !map_rows64(&mDY, dY, H, P) || !map_rows64(&mDG, dg, F, P) || !map_rows64(&mDU, du, F, P))
     return cudaErrorInvalidValue;
-  const bool deep = (long long)P >= (long long)MOE_WGRAD_PAIR_MIN_ROWS * E;
-  const bool pair = deep && H % 256 == 0 && F % 256 == 0;
+  // 256 x 256 tiles wherever the sizes allow: measured faster than the
+  // double-buffered 128-wide tiles from 32 to 1024 rows per expert, since the
+  // TMA-store epilogue keeps the unoverlapped part of a tile short.
+  const bool pair = H % 256 == 0 && F % 256 == 0;
   cudaError_t err = pair ? launch_w<1, true>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s)
                          : launch_w<1, false>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s);
   if (err != cudaSuccess) return err;
-  return (deep && H % 256 == 0)
+  return H % 256 == 0
              ? launch_w<2, true>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s)
              : launch_w<2, false>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s);
 }

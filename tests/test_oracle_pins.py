@@ -358,6 +358,29 @@ def test_backward_top1_has_no_logit_gradient():
     assert np.all(g["dlogits"] == 0)
 
 
+def test_backward_restrictions_for_sampling():
+    """The two restrictions a full-size check samples through: (a) a token's
+    dx and dlogits depend on that token alone (routing and combine are per
+    token), so the backward of a sub-batch gives the same rows; (b) SwiGLU
+    acts feature by feature, so the backward with F cut to a feature subset J
+    gives the dW1[:, :, J], dW3[:, :, J] and dW2[:, J, :] of the full one,
+    magnitudes included."""
+    T, H, F, E, k = 24, 6, 10, 5, 2
+    x, logits, W1, W3, W2 = rand_layer(T, H, F, E, k, seed=27)
+    dout = np.random.default_rng(28).standard_normal((T, H))
+    full = O.backward(x, logits, W1, W3, W2, k, dout, magnitudes=True)
+    tok = np.array([0, 5, 23])
+    sub = O.backward(x[tok], logits[tok], W1, W3, W2, k, dout[tok], magnitudes=True)
+    for n in ("dx", "dlogits", "mag_dx", "mag_dlogits"):
+        np.testing.assert_allclose(sub[n], full[n][tok], rtol=1e-12, atol=1e-14, err_msg=n)
+    J = np.array([0, 3, 9])
+    cut = O.backward(x, logits, W1[:, :, J], W3[:, :, J], W2[:, J, :], k, dout,
+                     magnitudes=True)
+    for n, sl in (("dW1", np.s_[:, :, J]), ("dW3", np.s_[:, :, J]), ("dW2", np.s_[:, J, :])):
+        for m in (n, "mag_" + n):
+            np.testing.assert_allclose(cut[m], full[m][sl], rtol=1e-12, atol=1e-14, err_msg=m)
+
+
 # ------------------------------------------------- the pages' own numbers
 def test_util_formula_a100_example():
     g = json.load(open(os.path.join(GOLDEN, "util_a100_example.json")))
