@@ -55,6 +55,7 @@ struct WCfg {
   static constexpr int kStages = kSmemBudget / kStageBytes;
   static constexpr int kAccCols = kMS * kNumB * kBN;
   static constexpr int kAccBufs = kPairM ? 1 : 2;
+  static constexpr int kRegions = kAccCols / 128;   // 128-column groups released one by one
   static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kStgOffset = kBarOffset + 1024;              // 1 KB-aligned for the swizzle
@@ -68,7 +69,7 @@ struct WBars {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_empty[2][4];   // per buffer, per 128-column group
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -118,7 +119,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&bars->acc_full[b], 1);
-      mbar_init(&bars->acc_empty[b], kEpiWarps);
+      for (int g = 0; g < C::kRegions; ++g) mbar_init(&bars->acc_empty[b][g], kEpiWarps);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -194,12 +195,17 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const WItem it = decode_witem<C::kTileRows, kBN>(w, n_m, n_n, offsets);
       const int nkb = (it.rows + BK - 1) / BK;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag,
-                                             kWaitLimitNs))) {
-        ok = false;
-        break;
+      // The accumulator's 128-column groups are handed back by the epilogue one
+      // at a time; the first stage of a tile waits for each group just before
+      // its first MMA, so the next tile starts while the last one is drained.
+      auto group_free = [&](int g) {
+        return __all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[acc][g], acc_phase ^ 1u,
+                                                 abort_flag, kWaitLimitNs));
+      };
+      if (nkb == 0) {   // an expert with no rows: nothing to accumulate
+        for (int g = 0; g < C::kRegions && ok; ++g) ok = group_free(g);
+        if (!ok) break;
       }
-      tc_fence_after();
       const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xffffffffu,
@@ -221,11 +227,32 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
         __syncwarp();
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
+        const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
+        if (kb == 0) {
+          // first stage: accumulator by accumulator, each once its columns are free
+          // (per accumulator the K order is the same as in the later stages)
+#pragma unroll
+          for (int t = 0; t < C::kMS * kNumB; ++t) {
+            const int ms = t / kNumB, b = t % kNumB;
+            for (int g = t * (kBN / 128); g < (t + 1) * (kBN / 128) && ok; ++g) ok = group_free(g);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t da = sdesc_sw128(a0 + ms * 2 * kBox + kk * 2048, kBox, 1024);
+                const uint64_t db =
+                    sdesc_sw128(a0 + C::kABytes + b * C::kBBytes + kk * 2048, kBox, 1024);
+                mma_bf16_ss(d0 + (uint32_t)(t * kBN), da, db, idesc, kk ? 1u : 0u);
+              }
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (lane == 0) mma_commit(&bars->empty[stage]);
+        } else if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t accum = (kb | kk) ? 1u : 0u;
             // both operands MN-major: 64-wide atoms 8 KB apart, 8-row groups 1 KB
             // apart, K step of 16 rows = 2 KB
 #pragma unroll
@@ -235,7 +262,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
               for (int b = 0; b < kNumB; ++b) {
                 const uint64_t db =
                     sdesc_sw128(a0 + C::kABytes + b * C::kBBytes + kk * 2048, kBox, 1024);
-                mma_bf16_ss(d0 + (uint32_t)((ms * kNumB + b) * kBN), da, db, idesc, accum);
+                mma_bf16_ss(d0 + (uint32_t)((ms * kNumB + b) * kBN), da, db, idesc, 1u);
               }
             }
           }
@@ -269,7 +296,6 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which alternate 64-column chunks it takes
     uint8_t* stg = smem + C::kStgOffset + (warp - 2) * kStgBytes;
-    constexpr int kChunks = C::kMS * kNumB * (kBN / 128);   // per warp per tile
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -282,13 +308,12 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      int chunk = 0;
 #pragma unroll
       for (int t = 0; t < C::kMS * kNumB; ++t) {
         const int ms = t / kNumB, b = t % kNumB;
         const int orow = it.e * M_total + it.m0 + ms * BM + q * 32;   // the warp's first row
 #pragma unroll
-        for (int c0 = 64 * half; c0 < kBN; c0 += 128, ++chunk) {
+        for (int c0 = 64 * half; c0 < kBN; c0 += 128) {
           uint32_t v[64];
           if (it.rows > 0) {
 #pragma unroll
@@ -300,11 +325,10 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 #pragma unroll
             for (int c = 0; c < 64; ++c) v[c] = 0u;
           }
-          if (chunk == kChunks - 1) {   // accumulator read out: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
-          }
+          // this warp's part of the 128-column group is read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty[acc][t * (kBN / 128) + c0 / 128]);
           if (lane == 0) bulk_wait_read_all();   // the previous store has left the buffer
           __syncwarp();
           // row `lane` of the box: 16-byte chunk j sits at j ^ (row & 7) (128B swizzle)
