@@ -100,28 +100,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                : "memory");
 }
 
-// Store a 2-D box from shared memory to global (bulk async-group of the
-// issuing thread); the shared source must be fenced for the async proxy.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
-                                             int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Until every committed store of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Until every committed store of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // L2 eviction-priority policies for the cache hints.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -85,11 +85,36 @@ __device__ __forceinline__ WItem decode_witem(int w, int n_m, int n_n, const int
   const int per = n_m * n_n;
   it.e = w / per;
   const int r = w - it.e * per;
-  it.m0 = (r / n_n) * kTileRows;
-  it.n0 = (r % n_n) * kBN;
+  // column tile outer, row tile inner: CTAs running side by side share one
+  // B column tile and sweep the expert's A rows, which stay in L2
+  it.n0 = (r / n_m) * kBN;
+  it.m0 = (r % n_m) * kTileRows;
   it.row0 = offsets[it.e];
   it.rows = offsets[it.e + 1] - it.row0;
   return it;
+}
+
+// Store a 2-D box from shared memory to global with an L2 cache hint (bulk
+// async-group of the issuing thread); the shared source must be fenced for
+// the async proxy first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until every committed store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Until every committed store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -296,6 +321,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which alternate 64-column chunks it takes
     uint8_t* stg = smem + C::kStgOffset + (warp - 2) * kStgBytes;
+    const uint64_t pol_out = policy_evict_first();   // written once, not read here
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -345,7 +371,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(b == 0 ? &tmO0 : &tmO1, stg, it.n0 + c0, orow);
+            tma_store_2d(b == 0 ? &tmO0 : &tmO1, stg, it.n0 + c0, orow, pol_out);
             bulk_commit();
           }
         }
