@@ -239,8 +239,11 @@ def bench_ours(args, rank, world, local):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {moe.moe_status_string(st)}")
 
+    # Timed region 1 (the value): K plain moe_forward steps.  With the L2 flush
+    # between steps, each step is bracketed by its own pair of events so the
+    # flush is not counted.
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+    step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
@@ -252,7 +255,10 @@ def bench_ours(args, rank, world, local):
     for i in range(K):
         if flush:
             flush_buf.zero_()
-        moe.moe_forward_events(x, logits, W1, W3, W2, wl.k, evs[i], out=out, ws=ws)
+            step_evs[i][0].record()
+        moe.moe_forward(x, logits, W1, W3, W2, wl.k, out=out, ws=ws)
+        if flush:
+            step_evs[i][1].record()
     t_end.record()
     barrier()
     if clocks:
@@ -260,15 +266,25 @@ def bench_ours(args, rank, world, local):
     st = moe.moe_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {moe.moe_status_string(st)}")
-
-    stage_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j in range(nst)]
-    step_ms = [evs[i][0].elapsed_time(evs[i][nst]) for i in range(K)]
-    total_ms = t_start.elapsed_time(t_end)
-    # With the L2 flush between steps the flush is not part of a step.
-    region_ms = sum(step_ms) if flush else total_ms
+    region_ms = (sum(e[0].elapsed_time(e[1]) for e in step_evs) if flush
+                 else t_start.elapsed_time(t_end))
     region_ms = max_over_ranks(region_ms, world, dev)
     ms_per_step = region_ms / K
     value = throughput(world, wl.T, K, region_ms)
+
+    # Timed region 2 (the per-kernel breakdown): K steps of moe_forward_events,
+    # one event between consecutive kernels on the launch stream.  The events
+    # themselves cost a few microseconds per step, which is why the value
+    # above comes from the region without them.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+    barrier()
+    for i in range(K):
+        if flush:
+            flush_buf.zero_()
+        moe.moe_forward_events(x, logits, W1, W3, W2, wl.k, evs[i], out=out, ws=ws)
+    barrier()
+    stage_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j in range(nst)]
+    events_ms_per_step = statistics.fmean(evs[i][0].elapsed_time(evs[i][nst]) for i in range(K))
 
     # end to end: host activations in, host result out, through the C ABI
     e2e = None
@@ -357,6 +373,9 @@ def bench_ours(args, rank, world, local):
         "roofline": roof,
         "layer_roofline": layer,
         "kernels": kernels,
+        "kernels_timing": ("per-stage CUDA events on the launch stream, in a second timed "
+                           f"region of {K} moe_forward_events steps "
+                           f"({events_ms_per_step:.4f} ms per step with the events)"),
         "gpu_launches": nst * K,
         "clocks": clocks.summary() if clocks else None,
     }
