@@ -76,6 +76,11 @@ struct Cfg {
   static constexpr int kStages = kSmemBudget / kStageBytes;
   static constexpr int kAccCols = kNumA * kBN;            // fp32 columns per buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols;
+  // With a single accumulator buffer, the epilogue hands its token columns back
+  // in groups of 64 and the next tile's first-stage MMAs wait only for the
+  // group they write, so the epilogue overlaps the next tile's main loop.
+  static constexpr int kRegions = kAccBufs == 1 ? kBN / 64 : 0;
+  static_assert(kRegions <= 4, "region barriers");
   static constexpr int kFeatPerItem = kGLU ? BM : kNumA * BM;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
@@ -91,6 +96,7 @@ struct Bars {
   uint64_t empty[8];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t acc_region[4];   // one accumulator buffer: its 64-token-column groups
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -164,6 +170,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       mbar_init(&bars->acc_full[b], 1);
       mbar_init(&bars->acc_empty[b], kEpiWarps);   // one arrival per epilogue warp
     }
+    for (int r = 0; r < C::kRegions; ++r) mbar_init(&bars->acc_region[r], kEpiWarps);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -256,11 +263,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int n = (it.nrows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n, /*a_mn=*/!kAKMajor, /*b_mn=*/false);
-        if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
+        if constexpr (kAccBufs == 2) {
+          if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
         for (int kb = 0; kb < nkb_all; ++kb) {
           if (!mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs)) {
@@ -270,6 +279,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
           const uint32_t b0 = a0 + (uint32_t)(kNumA * kABytes);
+          if (C::kRegions > 0 && kb == 0) {
+            // First stage, one 64-token-column group at a time, each once the
+            // epilogue has read it out of the previous tile.  Per accumulator
+            // element the K order is the same as in the later stages.
+            for (int r = 0; r < C::kRegions; ++r) {
+              if (!mbar_wait(&bars->acc_region[r], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const int c = 64 * r;
+              if (c >= n) continue;
+              const int nr = n - c < 64 ? n - c : 64;
+              const uint32_t idesc_r = idesc_bf16(BM, nr, /*a_mn=*/!kAKMajor, /*b_mn=*/false);
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                // token row c starts c * 128 bytes into the K-major N operand
+                const uint64_t db = sdesc_sw128(b0 + c * 128 + kk * 32, 16, 1024);
+#pragma unroll
+                for (int a = 0; a < kNumA; ++a) {
+                  const uint64_t da =
+                      kAKMajor ? sdesc_sw128(a0 + a * kABytes + kk * 32, 16, 1024)
+                               : sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024);
+                  mma_bf16_ss(d0 + (uint32_t)(a * kBN + c), da, db, idesc_r, kk ? 1u : 0u);
+                }
+              }
+            }
+            if (!ok) break;
+          } else {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
@@ -285,6 +323,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                            : sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024);
               mma_bf16_ss(d0 + (uint32_t)(a * kBN), da, db, idesc, accum);
             }
+          }
           }
           mma_commit(&bars->empty[stage]);
           if (++stage == C::kStages) {
@@ -325,7 +364,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       tc_fence_after();
       const int feat = it.mt * C::kFeatPerItem + q * 32 + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
+      // one 16-column chunk of the accumulator: TMEM -> registers -> epilogue
+      auto chunk = [&](int c0) {
         uint32_t g[16], g2[16];
         float pg[kNumA][16], pu[kNumA][16];
         if constexpr (kEpi == kEpiSwigluBwd) {
@@ -376,10 +416,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if constexpr (kNumA == 2) o[BM] = __float2bfloat16_rn(__uint_as_float(g2[c]));
           }
         }
+      };
+      if constexpr (C::kRegions > 0) {
+        // hand each 64-column group back as soon as this warp has read it
+        for (int r = 0; r < C::kRegions; ++r) {
+          for (int c0 = 64 * r + 16 * half; c0 < 64 * r + 64; c0 += 32)
+            if (c0 < it.nrows) chunk(c0);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_region[r]);
+        }
+      } else {
+        for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) chunk(c0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+
       if (++acc == kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
