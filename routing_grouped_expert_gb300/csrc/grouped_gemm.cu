@@ -48,7 +48,9 @@ constexpr int kABytes = BM * BK * 2;              // 16 KB per weight tile per s
 constexpr int kBBoxBytes = kRowBox * BK * 2;      // 32 token rows: 4 KB
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kSmemBudget = 204800;               // operand ring: 200 KB
+constexpr int kSmemBudget = 204800;               // operand ring: at most 200 KB
+constexpr int kSmemMax = 232448;                  // dynamic shared memory per CTA (227 KB)
+constexpr int kStgBox = 16 * 32 * 2;              // epilogue store box: 16 rows x 32 features
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 // What the epilogue does with the fp32 accumulators.
@@ -73,7 +75,21 @@ struct Cfg {
   static constexpr bool kGLU = kEpi == kEpiSwiglu || kEpi == kEpiSwigluSave;
   static constexpr int kBBytes = kBN * BK * 2;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
-  static constexpr int kStages = kSmemBudget / kStageBytes;
+  // bf16 outputs per accumulator column: each leaves through a 16-row x
+  // 32-feature staging box (1 KB per warp) and a TMA store
+  static constexpr int kOuts = kEpi == kEpiSwiglu ? 1 : kEpi == kEpiSwigluSave ? 3
+                             : kEpi == kEpiBf16 ? kNumA : kEpi == kEpiSwigluBwd ? 2 * kNumA : 0;
+  static constexpr int kStgSet = kOuts * kStgBox;   // one chunk's boxes
+  static constexpr int ring_stages(int slots) {
+    return kSmemBudget / kStageBytes < (kSmemMax - 2048 - kEpiWarps * slots * kStgSet) / kStageBytes
+               ? kSmemBudget / kStageBytes
+               : (kSmemMax - 2048 - kEpiWarps * slots * kStgSet) / kStageBytes;
+  }
+  // two staging sets per warp (a chunk is staged while the previous one is
+  // still being stored) when that costs no operand stage, else one
+  static constexpr int kStgSlots = ring_stages(2) == ring_stages(1) ? 2 : 1;
+  static constexpr int kStgPerWarp = kStgSlots * kStgSet;
+  static constexpr int kStages = ring_stages(kStgSlots);
   static constexpr int kAccCols = kNumA * kBN;            // fp32 columns per buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols;
   // With a single accumulator buffer, the epilogue hands its token columns back
@@ -83,7 +99,9 @@ struct Cfg {
   static_assert(kRegions <= 4, "region barriers");
   static constexpr int kFeatPerItem = kGLU ? BM : kNumA * BM;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+  static constexpr int kStgOffset = kBarOffset + 1024;
+  static constexpr int kSmemBytes = kStgOffset + kEpiWarps * kStgPerWarp + 1024;
+  static_assert(kSmemBytes <= kSmemMax, "shared memory per CTA");
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
@@ -139,6 +157,34 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   return it;
 }
 
+// Tensor maps of the bf16 outputs ([rows, ld], boxes of 16 rows x 32 features):
+// h / y / dx, or h, g, u (forward with saves), or dg, du (SwiGLU backward).
+struct OutMaps {
+  CUtensorMap m[3];
+};
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
+                   "l"(reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until at most kPending committed stores of this thread still read shared memory.
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
@@ -149,7 +195,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
                     void* __restrict__ out_ptr, int ld_out, int m_valid, EpiAux aux,
-                    int* __restrict__ status) {
+                    const __grid_constant__ OutMaps outs, int* __restrict__ status) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   constexpr bool kGLU = C::kGLU;
   extern __shared__ uint8_t smem_raw[];
@@ -351,6 +397,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which alternate 16-column chunks it takes
+    uint8_t* stg = smem + C::kStgOffset + (warp - 2) * C::kStgPerWarp;
+    int slot = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -362,7 +410,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         break;
       }
       tc_fence_after();
-      const int feat = it.mt * C::kFeatPerItem + q * 32 + lane;
+      const int wfeat = it.mt * C::kFeatPerItem + q * 32;   // the warp's first feature
+      const int feat = wfeat + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       // one 16-column chunk of the accumulator: TMEM -> registers -> epilogue
       auto chunk = [&](int c0) {
@@ -384,6 +433,60 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_ld_32x32b_x16(tb + c0, g);
         if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
         tmem_ld_wait();
+        if constexpr (C::kOuts > 0) {
+          if (c0 + 16 <= it.nrows) {
+            // a whole 16-row chunk: stage [row][feature] boxes, one TMA store each
+            // this staging set's previous boxes have left shared memory
+            if (lane == 0) bulk_wait_read<C::kStgSlots - 1>();
+            __syncwarp();
+            uint8_t* const set = stg + slot * C::kStgSet;
+            slot = slot + 1 == C::kStgSlots ? 0 : slot + 1;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float a0 = __uint_as_float(g[c]);
+              float v[C::kOuts];
+              if constexpr (kGLU) {
+                const float a1 = __uint_as_float(g2[c]);
+                v[0] = __fdividef(a0 * a1, 1.0f + __expf(-a0));
+                if constexpr (kEpi == kEpiSwigluSave) {
+                  v[1] = a0;
+                  v[2] = a1;
+                }
+              } else if constexpr (kEpi == kEpiSwigluBwd) {
+#pragma unroll
+                for (int a = 0; a < kNumA; ++a) {
+                  const float dh = a == 0 ? a0 : __uint_as_float(g2[c]);
+                  const float gv = pg[a][c], uv = pu[a][c];
+                  const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+                  v[2 * a] = dh * uv * sg * (1.0f + gv * (1.0f - sg));
+                  v[2 * a + 1] = dh * gv * sg;
+                }
+              } else {
+                v[0] = a0;
+                if constexpr (kNumA == 2) v[1] = __uint_as_float(g2[c]);
+              }
+#pragma unroll
+              for (int j = 0; j < C::kOuts; ++j)
+                *reinterpret_cast<__nv_bfloat16*>(set + j * kStgBox + c * 64 + lane * 2) =
+                    __float2bfloat16_rn(v[j]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int y = it.row0 + c0;
+#pragma unroll
+              for (int j = 0; j < C::kOuts; ++j) {
+                // output j: which map, and its feature offset
+                const int mi = kEpi == kEpiSwigluSave ? j : kEpi == kEpiSwigluBwd ? (j & 1) : 0;
+                const int xo = kEpi == kEpiSwigluBwd ? (j >> 1) * BM
+                             : kEpi == kEpiBf16 ? j * BM : 0;
+                tma_store_2d(&outs.m[mi], set + j * kStgBox, wfeat + xo, y);
+              }
+              bulk_commit();
+            }
+            return;
+          }
+        }
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           if (c0 + c >= it.nrows) continue;
@@ -438,9 +541,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         acc_phase ^= 1u;
       }
     }
-    if (!ok && lane == 0) {
-      set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
-      *abort_flag = 1;
+    if (lane == 0) {
+      if constexpr (C::kOuts > 0) bulk_wait_all();   // every staged box written
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
+        *abort_flag = 1;
+      }
     }
   }
 
@@ -473,13 +579,23 @@ EncodeTiledFn encode_fn() {
 
 // bf16 tensor map with a 128-byte swizzle; dims/strides innermost first.
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A bf16 output [rows, ld] (ld contiguous) as store boxes of 16 rows x 32
+// features, unswizzled (the epilogue stages rows of 64 bytes).
+bool map_out(CUtensorMap* m, const void* Y, int ld, int rows) {
+  const cuuint64_t d[2] = {(cuuint64_t)ld, (cuuint64_t)rows};
+  const cuuint64_t st[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {32, 16};
+  return make_map(m, Y, 2, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -499,7 +615,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const CUtensorMap& b1, const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
-                        int* status, cudaStream_t s) {
+                        const OutMaps& outs, int* status, cudaStream_t s) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   cudaError_t err =
@@ -512,7 +628,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, b1, offsets, block_off, num_blocks,
                                              block_expert, n_mt, K, out, ld_out, M_total, aux,
-                                             status);
+                                             outs, status);
   return cudaGetLastError();
 }
 
@@ -559,22 +675,29 @@ cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUt
                        const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
                        const EpiAux* save, int* status, cudaStream_t s) {
   const long long nb_max = max_blocks(P, E, kBN);
-  if (save != nullptr)
+  OutMaps om;
+  if (!map_out(&om.m[0], h, F, P)) return cudaErrorInvalidValue;
+  if (save != nullptr) {
+    if (!map_out(&om.m[1], save->g, save->ld, P) || !map_out(&om.m[2], save->u, save->ld, P))
+      return cudaErrorInvalidValue;
     return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
                                                        pl.num_blocks, pl.block_expert, F, H,
-                                                       nb_max, h, F, *save, status, s);
+                                                       nb_max, h, F, *save, om, status, s);
+  }
   return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
                                                  pl.num_blocks, pl.block_expert, F, H, nb_max, h,
-                                                 F, EpiAux{}, status, s);
+                                                 F, EpiAux{}, om, status, s);
 }
 
 template <int kNumA, int kBN, int kBufs>
 cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const PlanPtrs& pl, int P,
                        int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s) {
+  OutMaps om;
+  if (!map_out(&om.m[0], y, H, P)) return cudaErrorInvalidValue;
   return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(mW2, mW2, mH, mH, pl.offsets, pl.block_off,
                                                   pl.num_blocks, pl.block_expert, H, F,
-                                                  max_blocks(P, E, kBN), y, H, EpiAux{}, status,
-                                                  s);
+                                                  max_blocks(P, E, kBN), y, H, EpiAux{}, om,
+                                                  status, s);
 }
 
 // kPairF / kPairH: pair adjacent weight tiles (single-buffered accumulators)
@@ -590,14 +713,18 @@ cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
   constexpr int kAF = kPairF ? 2 : 1, kBufF = kPairF ? 1 : 2;
   constexpr int kAH = kPairH ? 2 : 1, kBufH = kPairH ? 1 : 2;
   // dh = dY W2[e]^T (M = F, K = H), then the SwiGLU derivative -> dg, du
+  OutMaps oh, ox;
+  if (!map_out(&oh.m[0], aux.dg, aux.ld, P) || !map_out(&oh.m[1], aux.du, aux.ld, P) ||
+      !map_out(&ox.m[0], dx_perm, H, P))
+    return cudaErrorInvalidValue;
   cudaError_t err = launch_gemm<kAF, kEpiSwigluBwd, kBN, kBufF, true>(
       mW2k, mW2k, mDY, mDY, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H,
-      nb_max, nullptr, 0, aux, status, s);
+      nb_max, nullptr, 0, aux, oh, status, s);
   if (err != cudaSuccess) return err;
   // dx_perm = dg W1[e]^T + du W3[e]^T (M = H, K = F in two phases)
   return launch_gemm<kAH, kEpiBf16, kBN, kBufH, true, true>(
       mW1k, mW3k, mDG, mDU, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
-      nb_max, dx_perm, H, EpiAux{}, status, s);
+      nb_max, dx_perm, H, EpiAux{}, ox, status, s);
 }
 
 }  // namespace
@@ -697,16 +824,16 @@ cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, 
       return launch_gemm<1, kEpiF32, kBlockRowsTiny, 2>(mG, mG, mX, mX, pl.offsets, pl.block_off,
                                                         pl.num_blocks, pl.block_expert, E, H,
                                                         max_blocks(T, 1, kBlockRowsTiny), logits,
-                                                        E, EpiAux{}, status, s);
+                                                        E, EpiAux{}, OutMaps{}, status, s);
     case FfnMode::kSmall:
       return launch_gemm<1, kEpiF32, kBlockRows, 2>(mG, mG, mX, mX, pl.offsets, pl.block_off,
                                                     pl.num_blocks, pl.block_expert, E, H,
                                                     max_blocks(T, 1, kBlockRows), logits, E,
-                                                    EpiAux{}, status, s);
+                                                    EpiAux{}, OutMaps{}, status, s);
     default:
       return launch_gemm<1, kEpiF32, kBlockRowsLarge, 2>(
           mG, mG, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, E, H,
-          max_blocks(T, 1, kBlockRowsLarge), logits, E, EpiAux{}, status, s);
+          max_blocks(T, 1, kBlockRowsLarge), logits, E, EpiAux{}, OutMaps{}, status, s);
   }
 }
 
