@@ -65,3 +65,42 @@ def test_gated_layer_matches_oracle(name):
     plain = moe.moe_forward_gated(dev["x"], dev["Wg"], dev["W1"], dev["W3"], dev["W2"], wl.k)
     again = moe.moe_forward(dev["x"], logits, dev["W1"], dev["W3"], dev["W2"], wl.k)
     assert torch.equal(plain, again)
+
+
+FULL = {  # workload of record, shared-expert width (0 = none)
+    "mixtral_decode": 0,        # E = 8: the SIMT router
+    "dbrx_prefill": 0,          # E = 16
+    "fine_grained": 2048,       # E = 256: the tensor-core router, plus a shared expert
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_gated_layer_full_size(name):
+    """Full sizes, launched as the gated benchmark launches them: every logit
+    against the fp64 product; the output on sampled tokens against the routed
+    per-token definition (ranked on the GPU's own fp32 logits) plus the shared
+    expert of those tokens."""
+    wl, Fs = I.WORKLOADS[name], FULL[name]
+    d = I.make_inputs(wl, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(6)
+    Wg = (torch.randn(wl.H, wl.E, generator=g, device="cuda") / math.sqrt(wl.H)).to(
+        torch.bfloat16)
+    shared = None
+    if Fs:
+        shared = tuple((torch.randn(r, c, generator=g, device="cuda") / math.sqrt(r)).to(
+            torch.bfloat16) for r, c in ((wl.H, Fs), (wl.H, Fs), (Fs, wl.H)))
+    ws = moe.Workspace()
+    out = moe.moe_forward_gated(d["x"], Wg, d["W1"], d["W3"], d["W2"], wl.k, shared=shared,
+                                ws=ws)
+    assert moe.moe_get_device_status(ws) == 0
+    logits = moe.moe_router_logits(d["x"], Wg)
+    ref_l = O.router_logits(d["x"].cpu(), Wg.cpu())
+    err = np.abs(logits.double().cpu().numpy() - ref_l)
+    assert np.all(err <= LOGIT_ATOL + LOGIT_RTOL * np.abs(ref_l)), err.max()
+    rng = np.random.default_rng(2)
+    tok = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, 4, replace=False)]))
+    ref = O.forward_direct(d["x"], logits.cpu().numpy(), d["W1"], d["W3"], d["W2"], wl.k,
+                           tokens=tok)
+    if shared is not None:
+        ref = ref + O.expert_ffn(d["x"][torch.from_numpy(tok).cuda()], *shared)
+    assert_moe_close(out[torch.from_numpy(tok).cuda()], ref, f"{name} gated out")
