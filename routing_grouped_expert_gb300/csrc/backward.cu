@@ -13,29 +13,46 @@ namespace {
 
 constexpr int kDwThreads = 128;
 
-// dY[p] = bf16(w[a] * dout[a / k]), a = sorted_src[p]; grid-stride, 16-byte vectors.
+// dY[p] = bf16(w[a] * dout[a / k]), a = sorted_src[p]: one warp per segment of
+// 4 x 32 16-byte vectors of a row, all four loads of a lane in flight before
+// its stores.
+constexpr int kScaleUnroll = 4;
 __global__ void __launch_bounds__(256)
 scale_gather_kernel(const __nv_bfloat16* __restrict__ dout, const int32_t* __restrict__ sorted_src,
                     const float* __restrict__ topk_w, int P, int H, int k,
                     __nv_bfloat16* __restrict__ dY) {
   const int nv = H / 8;
-  const long long total = (long long)P * nv;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(i / nv);
-    const int v = (int)(i - (long long)p * nv);
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int upr = (nv + 32 * kScaleUnroll - 1) / (32 * kScaleUnroll);   // segments per row
+  const long long units = (long long)P * upr;
+  for (long long wu = blockIdx.x * wpb + (threadIdx.x >> 5); wu < units;
+       wu += (long long)gridDim.x * wpb) {
+    const int p = (int)(wu / upr);
+    const int v0 = (int)(wu - (long long)p * upr) * 32 * kScaleUnroll + lane;
     const int a = __ldg(sorted_src + p);
     const float w = __ldg(topk_w + a);
-    const int4 raw = __ldg(reinterpret_cast<const int4*>(dout + (size_t)(a / k) * H) + v);
-    const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    int4 o;
-    __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
+    const int4* src = reinterpret_cast<const int4*>(dout + (size_t)(a / k) * H);
+    int4* dst = reinterpret_cast<int4*>(dY + (size_t)p * H);
+    {
+      int4 r[kScaleUnroll];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float2 f = __bfloat1622float2(in[c]);
-      po[c] = __floats2bfloat162_rn(w * f.x, w * f.y);
+      for (int u = 0; u < kScaleUnroll; ++u)
+        if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kScaleUnroll; ++u) {
+        if (v0 + 32 * u >= nv) continue;
+        const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&r[u]);
+        int4 o;
+        __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float2 f = __bfloat1622float2(in[c]);
+          po[c] = __floats2bfloat162_rn(w * f.x, w * f.y);
+        }
+        dst[v0 + 32 * u] = o;
+      }
     }
-    reinterpret_cast<int4*>(dY + (size_t)p * H)[v] = o;
   }
 }
 
@@ -120,9 +137,9 @@ cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* sorted
                                 const float* topk_w, int P, int H, int k, __nv_bfloat16* dY,
                                 cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  const long long vectors = (long long)P * (H / 8);
-  const long long want = (vectors + 255) / 256;
-  const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
+  const long long segs = (long long)P * ((H / 8 + 127) / 128);
+  const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
+  const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
   scale_gather_kernel<<<grid, 256, 0, s>>>(dout, sorted_src, topk_w, P, H, k, dY);
   return cudaGetLastError();
 }

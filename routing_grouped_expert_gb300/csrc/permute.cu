@@ -131,21 +131,33 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_ass
   }
 }
 
-// x_perm[p] = x[sorted_src[p] / k], 16-byte vectors, grid-stride over all
-// vectors of all rows so every SM takes part.
+// x_perm[p] = x[sorted_src[p] / k]: one warp per segment of 4 x 32 16-byte
+// vectors of a row (segments grid-strided), all four loads of a lane in
+// flight before its stores.
+constexpr int kGatherUnroll = 4;
 __global__ void __launch_bounds__(256)
 gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sorted_src, int P,
               int H, int k, __nv_bfloat16* __restrict__ x_perm) {
   const int nv = H / 8;
-  const long long total = (long long)P * nv;
-  const int4* src = reinterpret_cast<const int4*>(x);
-  int4* dst = reinterpret_cast<int4*>(x_perm);
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int row = (int)(i / nv);
-    const int v = (int)(i - (long long)row * nv);
-    const int t = __ldg(sorted_src + row) / k;
-    dst[i] = __ldg(src + (size_t)t * nv + v);
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int upr = (nv + 32 * kGatherUnroll - 1) / (32 * kGatherUnroll);   // segments per row
+  const long long units = (long long)P * upr;
+  for (long long w = blockIdx.x * wpb + (threadIdx.x >> 5); w < units;
+       w += (long long)gridDim.x * wpb) {
+    const int row = (int)(w / upr);
+    const int v0 = (int)(w - (long long)row * upr) * 32 * kGatherUnroll + lane;
+    const int4* src = reinterpret_cast<const int4*>(x) + (size_t)(__ldg(sorted_src + row) / k) * nv;
+    int4* dst = reinterpret_cast<int4*>(x_perm) + (size_t)row * nv;
+    {
+      int4 r[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (v0 + 32 * u < nv) dst[v0 + 32 * u] = r[u];
+    }
   }
 }
 
@@ -185,9 +197,9 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  const long long vectors = (long long)P * (H / 8);
-  const long long want = (vectors + 255) / 256;
-  const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
+  const long long segs = (long long)P * ((H / 8 + 127) / 128);
+  const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
+  const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
   gather_kernel<<<grid, 256, 0, s>>>(x, sorted_src, P, H, k, x_perm);
   return cudaGetLastError();
 }
