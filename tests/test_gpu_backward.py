@@ -33,6 +33,7 @@ CASES = {  # name: (T, H, F, E, k) -- block mode from the mean rows per expert
     "deep_wgrad_f384": (600, 256, 384, 2, 2),          # dW2 128-wide, dW1/dW3 256 x 256
     "many_empty_experts": (20, 128, 256, 32, 1),
     "fine_grained_like": (150, 256, 128, 32, 6),
+    "max_experts_topk": (64, 128, 128, 1024, 32),      # the header's limits
 }
 
 

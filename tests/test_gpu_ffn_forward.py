@@ -28,6 +28,8 @@ CASES = {  # name: (T, H, F, E, k, skew_alpha)
     "decode_long_k": (48, 256, 1024, 8, 2, 0.0),
     # more tokens than a grid's y dimension holds (65535)
     "many_tokens": (70000, 128, 128, 4, 1, 0.0),
+    # the header's limits: 1024 experts, top-32 (most experts get 0-4 rows)
+    "max_experts_topk": (64, 128, 128, 1024, 32, 0.0),
 }
 
 
