@@ -27,6 +27,8 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
                __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ y_shared) {
   __shared__ int s_row[MOE_MAX_TOPK];
   __shared__ float s_w[MOE_MAX_TOPK];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = dest_of[(size_t)t * k + threadIdx.x];
@@ -67,13 +69,12 @@ combine_kernel(const __nv_bfloat16* __restrict__ y_sorted, const int32_t* __rest
 
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
-                           cudaStream_t s, const __nv_bfloat16* y_shared) {
+                           cudaStream_t s, const __nv_bfloat16* y_shared, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int slices = (H / 8 + kCombineThreads - 1) / kCombineThreads;
   // tokens on the x dimension (up to 2^31 - 1), column slices on y
-  combine_kernel<<<dim3(T, slices), kCombineThreads, 0, s>>>(y_sorted, dest_of, topk_w, H, k,
-                                                            out, y_shared);
-  return cudaGetLastError();
+  return launch_k(combine_kernel, dim3(T, slices), dim3(kCombineThreads), 0, s, pdl, y_sorted,
+                  dest_of, topk_w, H, k, out, y_shared);
 }
 
 }  // namespace moe

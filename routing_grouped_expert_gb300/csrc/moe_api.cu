@@ -111,7 +111,12 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   __nv_bfloat16* y = ws_ptr<__nv_bfloat16>(ws, L.y);
 
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
-  // status word and the chunk histogram table (adjacent) start at zero
+  // The plain layer chains its short kernels (scan, scatter, gather, combine)
+  // by programmatic launch: each may start while its predecessor finishes (see
+  // pdl_wait).  The two persistent GEMMs keep stream order: measured, their
+  // statically scheduled CTAs gain nothing from starting early.  Stage events,
+  // the shared expert or the backward's saves keep plain ordering throughout.
+  const bool pdl = ev == nullptr && sh == nullptr && save == nullptr;
   // status word and the chunk histogram table (adjacent) start at zero
   if (clear)
     MOE_TRY(cudaMemsetAsync(status, 0,
@@ -120,11 +125,12 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
   MOE_TRY(mark(1));
   MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
-                      ffn_block_rows(P, E, H, F), s));
+                      ffn_block_rows(P, E, H, F), s, pdl));
   MOE_TRY(mark(2));
-  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
+  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s, pdl));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
+  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s,
+                        pdl));
   MOE_TRY(mark(4));
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),
@@ -140,7 +146,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                                sh->y, status, s));
   MOE_TRY(mark(6));
   MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
-                         sh ? sh->y : nullptr));
+                         sh ? sh->y : nullptr, pdl));
   MOE_TRY(mark(7));
   return MOE_OK;
 }

@@ -2,6 +2,8 @@
 // workspace layout, device status word, small device helpers.
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -177,25 +179,56 @@ inline GatedLayout gated_layout(int T, int H, int F, int Fs, int E, int k) {
 template <typename Tp>
 inline Tp* ws_ptr(void* ws, size_t off) { return reinterpret_cast<Tp*>((char*)ws + off); }
 
+// -------------------------------------------- programmatic dependent launch
+// The fused forward launches its chain of kernels with programmatic stream
+// serialisation: a kernel may start while its predecessor on the stream still
+// runs.  Such a kernel calls pdl_wait() before it touches memory that earlier
+// kernels of the chain write, and pdl_trigger() only after that wait, so that
+// when any kernel of the chain starts, every kernel before its direct
+// predecessor has completed.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? &attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------ launchers
-// Each returns cudaSuccess or the launch error.  All enqueue on `s`.
+// Each returns cudaSuccess or the launch error.  All enqueue on `s`; `pdl`
+// launches with programmatic stream serialisation (see above).
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
                          float* topk_w, int32_t* chunk_hist, int* status, cudaStream_t s);
 cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* chunk_hist,
                          int* status, cudaStream_t s);
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
-                        int beta, cudaStream_t s);
+                        int beta, cudaStream_t s, bool pdl = false);
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
-                           cudaStream_t s);
+                           cudaStream_t s, bool pdl = false);
 cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
                         int32_t* block_expert, int beta, cudaStream_t s);
 // Token-block rows (beta) the grouped FFN uses for a layer of these sizes;
 // the block plan must be built with the same value.
 int ffn_block_rows(int P, int E, int H, int F);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
-                          __nv_bfloat16* x_perm, cudaStream_t s);
+                          __nv_bfloat16* x_perm, cudaStream_t s, bool pdl = false);
 // Extra tensors of the grouped-GEMM epilogues that read or write more than
 // their main output.
 struct EpiAux {
@@ -226,7 +259,8 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
 // out[t] = sum_j w[t,j] y_sorted[dest_of[t*k+j]] (+ y_shared[t] when given)
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
-                           cudaStream_t s, const __nv_bfloat16* y_shared = nullptr);
+                           cudaStream_t s, const __nv_bfloat16* y_shared = nullptr,
+                           bool pdl = false);
 
 // Block plan of one expert that takes every token in order (router GEMM,
 // shared expert): offsets = {0, T}.

@@ -69,6 +69,8 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict_
             int32_t* __restrict__ offsets, int32_t* __restrict__ block_off,
             int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta) {
   __shared__ int warp_sums[33];
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
@@ -104,6 +106,8 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_ass
                const int32_t* __restrict__ chunk_base, int32_t* __restrict__ sorted_src,
                int32_t* __restrict__ dest_of) {
   extern __shared__ int cnt[];   // [warps][E]
+  pdl_wait();
+  pdl_trigger();
   const int nw = blockDim.x >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) cnt[i] = 0;
@@ -138,6 +142,8 @@ constexpr int kGatherUnroll = 4;
 __global__ void __launch_bounds__(256)
 gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sorted_src, int P,
               int H, int k, __nv_bfloat16* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   const int nv = H / 8;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -165,10 +171,9 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ s
 
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
-                        int beta, cudaStream_t s) {
-  scan_kernel<<<1, kScanThreads, 0, s>>>(chunk_hist, C, E, counts, offsets, block_off,
-                                         num_blocks, block_expert, beta);
-  return cudaGetLastError();
+                        int beta, cudaStream_t s, bool pdl) {
+  return launch_k(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, pdl, chunk_hist, C, E, counts,
+                  offsets, block_off, num_blocks, block_expert, beta);
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
@@ -179,7 +184,7 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32
 
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int C = num_chunks(T, k);
   const int chunk_assign = tokens_per_chunk(k) * k;
@@ -189,19 +194,18 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
       scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)((kChunkAssign / 32) * MOE_MAX_EXPERTS * sizeof(int)));
   if (err != cudaSuccess) return err;
-  scatter_kernel<<<C, kChunkAssign, smem, s>>>(topk_idx, T * k, E, chunk_assign, chunk_base,
-                                               sorted_src, dest_of);
-  return cudaGetLastError();
+  return launch_k(scatter_kernel, dim3(C), dim3(kChunkAssign), smem, s, pdl, topk_idx, T * k, E,
+                  chunk_assign, chunk_base, sorted_src, dest_of);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
-                          __nv_bfloat16* x_perm, cudaStream_t s) {
+                          __nv_bfloat16* x_perm, cudaStream_t s, bool pdl) {
   if (P == 0) return cudaSuccess;
   const long long segs = (long long)P * ((H / 8 + 127) / 128);
   const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
   const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
-  gather_kernel<<<grid, 256, 0, s>>>(x, sorted_src, P, H, k, x_perm);
-  return cudaGetLastError();
+  return launch_k(gather_kernel, dim3(grid), dim3(256), 0, s, pdl, x, sorted_src, P, H, k,
+                  x_perm);
 }
 
 }  // namespace moe

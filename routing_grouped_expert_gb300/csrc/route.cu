@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int tpc,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                   int32_t* __restrict__ chunk_hist, int* __restrict__ status) {
+  // first kernel of the fused chain (launched in stream order): the next one
+  // may start as soon as every CTA has begun; it waits for this one to finish
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * (kRouteThreads / 32) + warp;   // one token per warp
   if (t >= T) return;
