@@ -4,37 +4,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moe_common.cuh"
 
 namespace moe {
 
 namespace {
+// Per-device attributes, read once; callers may run on several host threads.
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];
-int g_is_sm103[kMaxDevices];   // 0 unknown, 1 yes, 2 no
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_is_sm103[kMaxDevices];   // 0 unknown, 1 yes, 2 no
 }  // namespace
 
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
-  if (g_sm_count[dev] == 0) {
+  int v = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_sm_count[dev] = n > 0 ? n : 1;
+    v = n > 0 ? n : 1;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return v;
 }
 
 bool device_is_sm103() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-  if (g_is_sm103[dev] == 0) {
+  int v = g_is_sm103[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    g_is_sm103[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    v = (major == 10 && minor == 3) ? 1 : 2;
+    g_is_sm103[dev].store(v, std::memory_order_relaxed);
   }
-  return g_is_sm103[dev] == 1;
+  return v == 1;
 }
 
 }  // namespace moe
