@@ -3,6 +3,8 @@
 // block plan and a status word -- lives in one fixed array in device memory
 // instead of a caller-supplied workspace.  The kernels are the same ones
 // moe_permute launches; only where their scratch lives differs.
+#include <atomic>
+
 #include "moe_common.cuh"
 
 // The scratch: MOE_PERMUTE_NOALLOC_SCRATCH_BYTES on every GPU on which the
@@ -17,7 +19,7 @@ constexpr size_t kScratchInts = MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / sizeof(int32
 constexpr int kMaxDevices = 64;
 // Device address of g_permute_scratch, looked up once per device.  In host
 // code the array's name is only a host-side stand-in, never a device pointer.
-int32_t* g_scratch_addr[kMaxDevices];
+std::atomic<int32_t*> g_scratch_addr[kMaxDevices];
 
 size_t round64(size_t v) { return (v + 63) / 64 * 64; }
 
@@ -33,13 +35,15 @@ cudaError_t scratch_address(int32_t** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (g_scratch_addr[dev] == nullptr) {
+  int32_t* a = g_scratch_addr[dev].load(std::memory_order_relaxed);
+  if (a == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_permute_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    a = static_cast<int32_t*>(p);
+    g_scratch_addr[dev].store(a, std::memory_order_relaxed);
   }
-  *out = g_scratch_addr[dev];
+  *out = a;
   return cudaSuccess;
 }
 
