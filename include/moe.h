@@ -182,13 +182,17 @@ moe_status moe_forward(const void* x, const float* router_logits,
                        void* ws, size_t ws_bytes, void* stream);
 
 /*
- * The whole layer with the per-step activations in HOST memory: copies
- * x_host [T, H] bf16 and logits_host [T, E] fp32 to the device, runs
- * moe_forward, and copies the result back to out_host [T, H] bf16.  The
- * weights are device pointers (resident model parameters).  Host buffers
- * should be page-locked for the copies to be asynchronous; out_host is
- * valid once `stream` has been synchronised.  The staging buffers live in
- * `ws` (moe_workspace_size covers them).
+ * The whole layer with the per-step activations in HOST memory: takes
+ * x_host [T, H] bf16 and logits_host [T, E] fp32, runs moe_forward and
+ * returns the result in out_host [T, H] bf16.  The weights are device
+ * pointers (resident model parameters).  A host buffer that is page-locked
+ * and mapped into the device's address space (cudaHostAlloc, cudaHostRegister,
+ * or a framework's pinned allocation) is used in place: the kernels read the
+ * logits and -- when T*k*H*2 is at most 32 MiB, since the gather reads each
+ * row of x k times -- x and the result across the host-device link, with no
+ * staging copy.  Any other host buffer is copied through a staging region of
+ * `ws` (moe_workspace_size covers it) with cudaMemcpyAsync.  out_host is
+ * valid once `stream` has been synchronised.
  */
 moe_status moe_forward_host(const void* x_host, const float* logits_host,
                             const void* W1, const void* W3, const void* W2,

@@ -296,6 +296,22 @@ const char* moe_forward_stage_name(int i) {
   return (i >= 0 && i < MOE_FORWARD_STAGES) ? kStageNames[i] : nullptr;
 }
 
+namespace {
+// The device address of a host buffer that kernels may access directly
+// (page-locked and mapped, 16-byte aligned), else nullptr.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // not a CUDA-known pointer: clear the error
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr ||
+      (reinterpret_cast<uintptr_t>(a.devicePointer) & 15u) != 0)
+    return nullptr;
+  return a.devicePointer;
+}
+}  // namespace
+
 moe_status moe_forward_host(const void* x_host, const float* logits_host, const void* W1,
                             const void* W3, const void* W2, int T, int H, int F, int E, int k,
                             void* out_host, void* ws, size_t ws_bytes, void* stream) {
@@ -308,14 +324,26 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
   if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* dx = ws_ptr<void>(ws, L.stage_x);
-  float* dl = ws_ptr<float>(ws, L.stage_logits);
-  void* dout = ws_ptr<void>(ws, L.stage_out);
-  MOE_TRY(cudaMemcpyAsync(dx, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s));
-  MOE_TRY(cudaMemcpyAsync(dl, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice, s));
+  // A page-locked, mapped host buffer is used in place: the kernels load the
+  // logits (each read once) and, for small batches, x and the result over the
+  // host link, with no staging copy.  The gather reads every row of x k times,
+  // so past kInPlaceBytes of gathered rows one copy into HBM is cheaper.  Any
+  // other host buffer goes through a staging region of ws.
+  constexpr size_t kInPlaceBytes = size_t(32) << 20;
+  const bool small = (size_t)T * k * H * 2 <= kInPlaceBytes;
+  void* xm = small ? mapped_host(x_host) : nullptr;
+  void* lm = mapped_host(logits_host);
+  void* om = small ? mapped_host(out_host) : nullptr;
+  void* dx = xm ? xm : ws_ptr<void>(ws, L.stage_x);
+  float* dl = lm ? static_cast<float*>(lm) : ws_ptr<float>(ws, L.stage_logits);
+  void* dout = om ? om : ws_ptr<void>(ws, L.stage_out);
+  if (!xm) MOE_TRY(cudaMemcpyAsync(dx, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s));
+  if (!lm)
+    MOE_TRY(cudaMemcpyAsync(dl, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice, s));
   const moe_status st = forward_device(dx, dl, W1, W3, W2, T, H, F, E, k, dout, ws, L, s);
   if (st != MOE_OK) return st;
-  MOE_TRY(cudaMemcpyAsync(out_host, dout, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s));
+  if (!om)
+    MOE_TRY(cudaMemcpyAsync(out_host, dout, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }
 

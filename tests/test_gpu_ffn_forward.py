@@ -90,6 +90,12 @@ def test_forward_host_matches_device(case):
     out_h = moe.moe_forward_host(xh, lh, dev["W1"], dev["W3"], dev["W2"], wl.k)
     torch.cuda.current_stream().synchronize()
     assert torch.equal(out_h, out_d.cpu())
+    # pageable buffers take the staging copies: same bits
+    out_p = torch.empty_like(out_h, device="cpu")
+    moe.moe_forward_host(d["x"].clone(), d["logits"].clone(), dev["W1"], dev["W3"], dev["W2"],
+                         wl.k, out_host=out_p)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out_p, out_d.cpu())
 
 
 def test_status_ok_after_forward(case):

@@ -45,3 +45,17 @@ def test_full_size_workload(name):
     counts = to_np(moe.moe_permute(idx, wl.E)[0])
     assert counts.sum() == wl.T * wl.k
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode", "dbrx_prefill"])
+def test_full_size_host_buffers(name):
+    """moe_forward_host with pinned host buffers gives moe_forward's bits: the
+    decode batch reads and writes them in place, the prefill chunk (past the
+    in-place size) stages them through the workspace."""
+    wl = I.WORKLOADS[name]
+    d = I.make_inputs(wl, "cuda")
+    out = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k)
+    xh, lh = d["x"].cpu().pin_memory(), d["logits"].cpu().pin_memory()
+    out_h = moe.moe_forward_host(xh, lh, d["W1"], d["W3"], d["W2"], wl.k)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out_h, out.cpu())
