@@ -325,15 +325,15 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // A page-locked, mapped host buffer is used in place: the kernels load the
-  // logits (each read once) and, for small batches, x and the result over the
-  // host link, with no staging copy.  The gather reads every row of x k times,
-  // so past kInPlaceBytes of gathered rows one copy into HBM is cheaper.  Any
-  // other host buffer goes through a staging region of ws.
+  // logits and store the result (each element once) and, for small batches,
+  // load x over the host link, with no staging copy.  The gather reads every
+  // row of x k times, so past kInPlaceBytes of gathered rows one copy into
+  // HBM is cheaper.  Any other host buffer goes through a staging region of ws.
   constexpr size_t kInPlaceBytes = size_t(32) << 20;
   const bool small = (size_t)T * k * H * 2 <= kInPlaceBytes;
   void* xm = small ? mapped_host(x_host) : nullptr;
   void* lm = mapped_host(logits_host);
-  void* om = small ? mapped_host(out_host) : nullptr;
+  void* om = mapped_host(out_host);   // the combine writes each result row once
   void* dx = xm ? xm : ws_ptr<void>(ws, L.stage_x);
   float* dl = lm ? static_cast<float*>(lm) : ws_ptr<float>(ws, L.stage_logits);
   void* dout = om ? om : ws_ptr<void>(ws, L.stage_out);
