@@ -50,8 +50,8 @@ def test_full_size_workload(name):
 @pytest.mark.parametrize("name", ["mixtral_decode", "dbrx_prefill"])
 def test_full_size_host_buffers(name):
     """moe_forward_host with pinned host buffers gives moe_forward's bits: the
-    decode batch reads and writes them in place, the prefill chunk (past the
-    in-place size) stages them through the workspace."""
+    decode batch reads x in place, the prefill chunk (past the in-place size)
+    stages x through the workspace; both write the result in place."""
     wl = I.WORKLOADS[name]
     d = I.make_inputs(wl, "cuda")
     out = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k)
