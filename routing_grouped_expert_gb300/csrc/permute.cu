@@ -72,13 +72,16 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict_
   pdl_wait();
   pdl_trigger();
   const int e = threadIdx.x;
+  constexpr int kBatch = 8;   // loads in flight per thread
   int cnt = 0;
   if (e < E) {
-    // prefix over chunks: chunk c's rows of expert e start after chunks < c
-    for (int c = 0; c < C; ++c) {
-      const int v = chunk_hist[(size_t)c * E + e];
-      chunk_hist[(size_t)c * E + e] = cnt;
-      cnt += v;
+    // the expert's count over all chunks (loads only, batched)
+    for (int c0 = 0; c0 < C; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) v[i] = c0 + i < C ? chunk_hist[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) cnt += v[i];
     }
   }
   int total;
@@ -86,7 +89,18 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict_
   if (e < E) {
     counts[e] = cnt;
     offsets[e] = off;
-    for (int c = 0; c < C; ++c) chunk_hist[(size_t)c * E + e] += off;
+    // chunk c's rows of expert e start at off + (its rows in chunks < c)
+    int run = off;
+    for (int c0 = 0; c0 < C; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) v[i] = c0 + i < C ? chunk_hist[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (c0 + i < C) chunk_hist[(size_t)(c0 + i) * E + e] = run;
+        run += v[i];
+      }
+    }
   }
   if (e == 0) offsets[E] = total;
   write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
