@@ -1,6 +1,8 @@
-"""The benchmark's multi-rank host logic on CPU ranks (gloo, world size 2):
-the slowest rank's time sets the whole-job throughput, and the reference arm
-runs on rank 0 only."""
+"""The multi-rank host logic on CPU ranks (gloo, world size 2): the slowest
+rank's time sets the benchmark's whole-job throughput, the reference arm runs
+on rank 0 only, and an expert-tensor-sharded layer (each rank holding a slice
+of every expert's FFN features) is recovered by one all-reduce of the ranks'
+partial outputs."""
 import os
 import socket
 
@@ -52,3 +54,40 @@ def test_single_rank_throughput():
     import bench
     assert bench.max_over_ranks(3.5, 1, None) == 3.5
     assert bench.throughput(1, 128, 500, 400.0) == pytest.approx(128 * 500 / 0.4)
+
+
+def _shard_worker(rank, world, port, q):
+    import numpy as np
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from oracle import moe_oracle as O
+    g = torch.Generator().manual_seed(3)
+    T, H, F, E, k = 24, 16, 32, 4, 2
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(E, H, F, generator=g) / 4).to(torch.bfloat16)
+    W3 = (torch.randn(E, H, F, generator=g) / 4).to(torch.bfloat16)
+    W2 = (torch.randn(E, F, H, generator=g) / 6).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g).numpy()
+    s = np.array_split(np.arange(F), world)[rank]     # this rank's features
+    part = O.forward_perm(x, logits, W1[:, :, s], W3[:, :, s], W2[:, s, :], k)["out"]
+    t = torch.from_numpy(np.ascontiguousarray(part))
+    dist.all_reduce(t)                                 # the one exchange step
+    full = O.forward_perm(x, logits, W1, W3, W2, k)["out"]
+    q.put((rank, float(np.abs(t.numpy() - full).max())))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_feature_sharded_layer_needs_one_all_reduce():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_shard_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, err in got:
+        assert err <= 1e-12

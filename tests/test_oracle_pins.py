@@ -381,6 +381,20 @@ def test_backward_restrictions_for_sampling():
             np.testing.assert_allclose(cut[m], full[m][sl], rtol=1e-12, atol=1e-14, err_msg=m)
 
 
+def test_layer_is_a_sum_over_ffn_feature_slices():
+    """Expert-tensor sharding along F ("MegaScale-Infer", §3.4, tpe): the
+    routing does not depend on the FFN width and SwiGLU acts feature by
+    feature, so the layer over W1[:, :, S], W3[:, :, S], W2[:, S, :] summed
+    over a partition of the features is the whole layer."""
+    x, logits, W1, W3, W2 = rand_layer(40, 16, 24, 5, 2, seed=29)
+    full = O.forward_perm(x, logits, W1, W3, W2, 2)["out"]
+    for parts in (2, 3):
+        S = np.array_split(np.arange(24), parts)
+        tot = sum(O.forward_perm(x, logits, W1[:, :, s], W3[:, :, s], W2[:, s, :], 2)["out"]
+                  for s in S)
+        np.testing.assert_allclose(tot, full, rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------- the pages' own numbers
 def test_util_formula_a100_example():
     g = json.load(open(os.path.join(GOLDEN, "util_a100_example.json")))
