@@ -115,9 +115,12 @@ struct Bars {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t acc_region[4];   // one accumulator buffer: its 64-token-column groups
+  uint64_t sk_written;      // split tiles: every epilogue warp stored its partial
+  uint64_t sk_decided;      // split tiles: whether this CTA finishes the tile
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int sk_last;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block too large");
 
@@ -157,6 +160,51 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   return it;
 }
 
+// Balanced K split ("stream-K") of a persistent grouped GEMM whose tile count
+// is not a multiple of the CTA count: the tiles' K stages are laid end to
+// end and each CTA takes an equal contiguous range, so a tile may be cut
+// between two neighbouring CTAs.  Each part stores its fp32 partial tile in
+// a slot of its own CTA and counts itself in at the boundary; the second to
+// arrive adds the other's partial (two-term fp32 sums commute, so the result
+// does not depend on which CTA finishes) and stores the tile.  Nothing waits
+// on another CTA.
+struct StreamK {
+  float* part;   // [CTAs][2][kTileM][kBN]: slot 0 the CTA's first part, 1 its last
+  int* cnt;      // [CTAs] arrivals at each CTA boundary, zero between launches
+};
+
+// The (tile, K-stage range) segments a CTA processes, in order.
+struct Segments {
+  long long u, end;   // stream-K: this CTA's range of (tile, stage) units
+  int w, step, total, nkb;
+  bool sk;
+  __device__ Segments(bool split_ok, int total_, int nkb_)
+      : w(blockIdx.x), step(gridDim.x), total(total_), nkb(nkb_) {
+    sk = split_ok && total > (int)gridDim.x && total % (int)gridDim.x != 0;
+    // (measured: ranges cut at any K stage balance best; rounding the cuts to
+    // 1/16 .. 1/4 of a tile was slower)
+    const long long U = (long long)total * nkb;
+    u = U * blockIdx.x / gridDim.x;
+    end = U * (blockIdx.x + 1) / gridDim.x;
+  }
+  __device__ bool next(int& wo, int& kb0, int& kb1) {
+    if (sk) {
+      if (u >= end) return false;
+      wo = (int)(u / nkb);
+      kb0 = (int)(u - (long long)wo * nkb);
+      kb1 = (int)min((long long)nkb, kb0 + (end - u));
+      u += kb1 - kb0;
+      return true;
+    }
+    if (w >= total) return false;
+    wo = w;
+    kb0 = 0;
+    kb1 = nkb;
+    w += step;
+    return true;
+  }
+};
+
 // Tensor maps of the bf16 outputs ([rows, ld], boxes of 16 rows x 32 features):
 // h / y / dx, or h, g, u (forward with saves), or dg, du (SwiGLU backward).
 struct OutMaps {
@@ -195,7 +243,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
                     void* __restrict__ out_ptr, int ld_out, int m_valid, EpiAux aux,
-                    const __grid_constant__ OutMaps outs, int* __restrict__ status) {
+                    const __grid_constant__ OutMaps outs, StreamK sk, int* __restrict__ status) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   constexpr bool kGLU = C::kGLU;
   extern __shared__ uint8_t smem_raw[];
@@ -204,6 +252,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = *num_blocks_ptr * n_mt;
+  // stream-K only for a single weight tile with two accumulator buffers and a
+  // bf16 output (FC2 of small token blocks)
+  constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2 && !kDualK;
+  const bool sk_ok = kSKCapable && sk.part != nullptr;
   const int nkb = K / BK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
 
@@ -217,6 +269,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       mbar_init(&bars->acc_empty[b], kEpiWarps);   // one arrival per epilogue warp
     }
     for (int r = 0; r < C::kRegions; ++r) mbar_init(&bars->acc_region[r], kEpiWarps);
+    mbar_init(&bars->sk_written, kEpiWarps);
+    mbar_init(&bars->sk_decided, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -249,13 +303,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      Segments sg(sk_ok, total, nkb_all);
+      int w, kb0, kb1;
+      while (ok && sg.next(w, kb0, kb1)) {
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
         const uint32_t bytes = kNumA * kABytes + nbox * kBBoxBytes;
         const int f0 = it.mt * C::kFeatPerItem;
         const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
-        for (int kb = 0; kb < nkb_all; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -305,7 +361,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      Segments sg(sk_ok, total, nkb_all);
+      int w, kb0, kb1;
+      while (ok && sg.next(w, kb0, kb1)) {
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int n = (it.nrows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(BM, n, /*a_mn=*/!kAKMajor, /*b_mn=*/false);
@@ -317,7 +375,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           tc_fence_after();
         }
         const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
-        for (int kb = 0; kb < nkb_all; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -325,7 +383,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
           const uint32_t b0 = a0 + (uint32_t)(kNumA * kABytes);
-          if (C::kRegions > 0 && kb == 0) {
+          if (C::kRegions > 0 && kb == kb0) {
             // First stage, one 64-token-column group at a time, each once the
             // epilogue has read it out of the previous tile.  Per accumulator
             // element the K order is the same as in the later stages.
@@ -356,7 +414,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           } else {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || kk) ? 1u : 0u;
             // N operand: K-major rows of 128 B; K step of 16 = 32 B inside the atom.
             const uint64_t db = sdesc_sw128(b0 + kk * 32, 16, 1024);
 #pragma unroll
@@ -402,7 +460,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    int sk_n = 0;   // split tiles this CTA has taken part in (phase of the sk barriers)
+    Segments sg(sk_ok, total, nkb_all);
+    int w, kb0, kb1;
+    while (sg.next(w, kb0, kb1)) {
       const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
       const bool got = mbar_wait(&bars->acc_full[acc], acc_phase, abort_flag, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, got)) {
@@ -413,6 +474,58 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       const int wfeat = it.mt * C::kFeatPerItem + q * 32;   // the warp's first feature
       const int feat = wfeat + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      // A tile cut between two CTAs: store this part, count in at the boundary;
+      // the second part to arrive adds the other's partial and stores the tile.
+      const float* other = nullptr;   // the neighbour's partial to add
+      bool store = true;
+      if constexpr (kSKCapable) {
+        if (kb0 > 0 || kb1 < nkb_all) {
+          const bool head = kb0 == 0;   // the tile's first stages: this CTA's last part
+          const int c = blockIdx.x;
+          float* mine = sk.part + ((size_t)c * 2 + (head ? 1 : 0)) * BM * kBN;
+          const float* theirs =
+              sk.part + (head ? (size_t)(c + 1) * 2 : (size_t)(c - 1) * 2 + 1) * BM * kBN;
+          int* cnt = sk.cnt + (head ? c : c - 1);
+          for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tb + c0, v);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(mine + (size_t)(q * 32 + lane) * kBN + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+          __threadfence();   // this thread's partial is visible device-wide
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->sk_written);
+          bool good = true;
+          if (warp == 2 && lane == 0) {
+            good = mbar_wait(&bars->sk_written, (uint32_t)(sk_n & 1), abort_flag, kWaitLimitNs);
+            int last = 0;
+            if (good) {
+              __threadfence();
+              last = atomicAdd(cnt, 1) == 1;
+              if (last) *cnt = 0;   // both parts counted: zero for the next launch
+            }
+            bars->sk_last = last;
+            mbar_arrive(&bars->sk_decided);
+          }
+          const bool dec =
+              mbar_wait(&bars->sk_decided, (uint32_t)(sk_n & 1), abort_flag, kWaitLimitNs);
+          ++sk_n;
+          if (!__all_sync(0xffffffffu, good && dec)) {
+            ok = false;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&bars->sk_last)) {
+            __threadfence();   // the neighbour's partial, published before its count
+            other = theirs;
+          } else {
+            store = false;
+          }
+        }
+      }
       // one 16-column chunk of the accumulator: TMEM -> registers -> epilogue
       auto chunk = [&](int c0) {
         uint32_t g[16], g2[16];
@@ -433,6 +546,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_ld_32x32b_x16(tb + c0, g);
         if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
         tmem_ld_wait();
+        if constexpr (kSKCapable) {
+          if (other != nullptr) {   // finish a cut tile: add the neighbour's part
+            const float4* o4 =
+                reinterpret_cast<const float4*>(other + (size_t)(q * 32 + lane) * kBN + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 t = __ldcg(o4 + j);
+              g[4 * j] = __float_as_uint(__uint_as_float(g[4 * j]) + t.x);
+              g[4 * j + 1] = __float_as_uint(__uint_as_float(g[4 * j + 1]) + t.y);
+              g[4 * j + 2] = __float_as_uint(__uint_as_float(g[4 * j + 2]) + t.z);
+              g[4 * j + 3] = __float_as_uint(__uint_as_float(g[4 * j + 3]) + t.w);
+            }
+          }
+        }
         if constexpr (C::kOuts > 0) {
           if (c0 + 16 <= it.nrows) {
             // a whole 16-row chunk: stage [row][feature] boxes, one TMA store each
@@ -530,7 +657,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           if (lane == 0) mbar_arrive(&bars->acc_region[r]);
         }
       } else {
-        for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) chunk(c0);
+        if (store)
+          for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) chunk(c0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
@@ -616,7 +744,8 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const CUtensorMap& b1, const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
-                        const OutMaps& outs, int* status, cudaStream_t s) {
+                        const OutMaps& outs, int* status, cudaStream_t s,
+                        StreamK sk = StreamK{nullptr, nullptr}) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   cudaError_t err =
@@ -627,9 +756,10 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   const int n_mt = (M_total + C::kFeatPerItem - 1) / C::kFeatPerItem;
   const long long items = nb_max * n_mt;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
+  if (grid > kStreamKMaxCtas) sk = StreamK{nullptr, nullptr};
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, b1, offsets, block_off, num_blocks,
                                              block_expert, n_mt, K, out, ld_out, M_total, aux,
-                                             outs, status);
+                                             outs, sk, status);
   return cudaGetLastError();
 }
 
@@ -692,13 +822,14 @@ cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUt
 
 template <int kNumA, int kBN, int kBufs>
 cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const PlanPtrs& pl, int P,
-                       int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s) {
+                       int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s,
+                       StreamK sk = StreamK{nullptr, nullptr}) {
   OutMaps om;
   if (!map_out(&om.m[0], y, H, P)) return cudaErrorInvalidValue;
   return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(mW2, mW2, mH, mH, pl.offsets, pl.block_off,
                                                   pl.num_blocks, pl.block_expert, H, F,
                                                   max_blocks(P, E, kBN), y, H, EpiAux{}, om,
-                                                  status, s);
+                                                  status, s, sk);
 }
 
 // kPairF / kPairH: pair adjacent weight tiles (single-buffered accumulators)
@@ -745,7 +876,8 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const int32_t* block_expert, const __nv_bfloat16* W1,
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
-                               cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save) {
+                               cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save,
+                               const StreamKSpace* sks) {
   if (P == 0) return cudaSuccess;
   CUtensorMap mW1, mW3, mW2, mX, mH;
   if (!map_weights_mn(&mW1, W1, H, F, E) || !map_weights_mn(&mW3, W3, H, F, E) ||
@@ -763,10 +895,12 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
     err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
+  // FC2 of small blocks: balanced K split when its tiles do not fill the SMs evenly
+  const StreamK sk = sks ? StreamK{sks->part, sks->cnt} : StreamK{nullptr, nullptr};
   if (mode == FfnMode::kTiny)
-    return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
+    return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   if (mode == FfnMode::kSmall)
-    return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
+    return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   if (fc2_paired(H, F))
     return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s);
   return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s);

@@ -139,18 +139,19 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s,
                         pdl));
   MOE_TRY(mark(4));
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
-                             ev ? ev[5] : nullptr, save));
+                             ev ? ev[5] : nullptr, save, &sks));
   if (sh != nullptr)
     MOE_TRY(launch_grouped_ffn(static_cast<const __nv_bfloat16*>(x), sh->plan.offsets,
                                sh->plan.block_off, sh->plan.num_blocks, sh->plan.block_expert,
                                static_cast<const __nv_bfloat16*>(sh->W1),
                                static_cast<const __nv_bfloat16*>(sh->W3),
                                static_cast<const __nv_bfloat16*>(sh->W2), T, H, sh->Fs, 1, sh->h,
-                               sh->y, status, s));
+                               sh->y, status, s, nullptr, nullptr, &sks));
   MOE_TRY(mark(6));
   MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
                          sh ? sh->y : nullptr, pdl));
@@ -230,7 +231,9 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
   int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
   __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
-  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
+  // the status word and FC2's split counters (adjacent) start at zero
+  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
   MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert,
                       ffn_block_rows(P, E, H, F), s));
   MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
@@ -239,7 +242,8 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E,
                              ws_ptr<__nv_bfloat16>(ws, L.h),
-                             static_cast<__nv_bfloat16*>(y_sorted), status, s));
+                             static_cast<__nv_bfloat16*>(y_sorted), status, s, nullptr, nullptr,
+                             &sks));
   return MOE_OK;
 }
 

@@ -68,8 +68,13 @@ __device__ __forceinline__ void set_status(int* status, int code, int detail = 0
 }
 
 // ------------------------------------------------------ workspace layout
+// CTAs whose FC2 partial tiles the workspace has room for (a launch with a
+// larger grid does not split tiles).
+constexpr int kStreamKMaxCtas = 256;
+
 struct WsLayout {
   size_t status;        // int32[64]
+  size_t sk_cnt;        // int32[kStreamKMaxCtas]   FC2 split counters (cleared with status)
   size_t topk_idx;      // int32[P]
   size_t topk_w;        // f32[P]
   size_t counts;        // int32[E]
@@ -83,6 +88,7 @@ struct WsLayout {
   size_t x_perm;        // bf16[P*H]
   size_t h;             // bf16[P*F]
   size_t y;             // bf16[P*H]
+  size_t sk_part;       // f32[kStreamKMaxCtas*2*kTileM*kBlockRows]   FC2 split partials
   size_t stage_x;       // bf16[T*H]   device staging for moe_forward_host
   size_t stage_logits;  // f32[T*E]
   size_t stage_out;     // bf16[T*H]
@@ -124,7 +130,8 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
   L.status = take(64 * 4);
-  L.chunk_base = take(C * E * 4);   // right after the status: one memset clears both
+  L.sk_cnt = take((size_t)kStreamKMaxCtas * 4);
+  L.chunk_base = take(C * E * 4);   // after status and sk_cnt: one memset clears all three
   L.topk_idx = take(P * 4);
   L.topk_w = take(P * 4);
   L.counts = take((size_t)E * 4);
@@ -137,7 +144,8 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   L.x_perm = take(P * H * 2);
   L.h = take(P * F * 2);
   L.y = take(P * H * 2);
-  L.stage_x = take((size_t)T * H * 2);
+  L.sk_part = take((size_t)kStreamKMaxCtas * 2 * kTileM * kBlockRows * 4);
+  L.stage_x = take((size_t)T * H * 2);   // the host-buffer staging comes last
   L.stage_logits = take((size_t)T * E * 4);
   L.stage_out = take((size_t)T * H * 2);
   L.total = o;
@@ -238,6 +246,12 @@ struct EpiAux {
   __nv_bfloat16* du;
   int ld;
 };
+// Scratch of FC2's balanced K split: partial tiles and boundary counters.  The
+// counters must be zero before a launch; every launch leaves them zero.
+struct StreamKSpace {
+  float* part;   // [kStreamKMaxCtas][2][kTileM][kBlockRows] fp32
+  int* cnt;      // [kStreamKMaxCtas]
+};
 // FC1 (+SwiGLU) and FC2 over the expert groups.  With `save`, FC1 also keeps
 // its pre-activations g = x W1, u = x W3 (bf16, [P, F]) for the backward.
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
@@ -246,7 +260,8 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
                                cudaStream_t s, cudaEvent_t after_fc1 = nullptr,
-                               const EpiAux* save = nullptr);
+                               const EpiAux* save = nullptr,
+                               const StreamKSpace* sks = nullptr);
 // Backward DGrad of both expert GEMMs: dh = dY W2^T -> dg, du (SwiGLU
 // derivative from the saved g, u), dx_perm = dg W1^T + du W3^T.
 cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,

@@ -30,6 +30,10 @@ CASES = {  # name: (T, H, F, E, k, skew_alpha)
     "many_tokens": (70000, 128, 128, 4, 1, 0.0),
     # the header's limits: 1024 experts, top-32 (most experts get 0-4 rows)
     "max_experts_topk": (64, 128, 128, 1024, 32, 0.0),
+    # FC2 tiles (320) not a multiple of the SMs: a balanced K split cuts some
+    # tiles between two CTAs (64- and 128-row blocks)
+    "split_fc2_tiny": (64, 2560, 1024, 16, 2, 0.0),
+    "split_fc2_small": (400, 2560, 512, 16, 2, 0.0),
 }
 
 
