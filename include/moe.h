@@ -23,8 +23,11 @@
  *     except moe_get_device_status.
  *   - `ws` is a caller-owned device workspace of at least
  *     moe_workspace_size(T, H, F, E, k) bytes, 256-byte aligned.  It holds
- *     the intermediates and a device status word.  Calls that share one
- *     workspace must not overlap in time (use one stream per workspace).
+ *     the intermediates (gathered rows, expert activations and outputs), a
+ *     fixed 32 MiB of partial tiles for the balanced K split of FC2, and a
+ *     device status word.  Its contents need no initialisation.  Calls that
+ *     share one workspace must not overlap in time (use one stream per
+ *     workspace).
  *   - Limits: 0 <= T, T*k < 2^31; 1 <= E <= MOE_MAX_EXPERTS;
  *     1 <= k <= min(E, MOE_MAX_TOPK); H and F positive multiples of 128.
  *     Violations are reported synchronously as MOE_ERR_INVALID_ARG and
