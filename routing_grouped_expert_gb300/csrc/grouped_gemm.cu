@@ -253,8 +253,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = *num_blocks_ptr * n_mt;
   // stream-K only for a single weight tile with two accumulator buffers and a
-  // bf16 output (FC2 of small token blocks)
-  constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2 && !kDualK;
+  // bf16 output (FC2 and DGrad dx of small token blocks)
+  constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2;
   const bool sk_ok = kSKCapable && sk.part != nullptr;
   const int nkb = K / BK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
@@ -840,7 +840,8 @@ cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
                            const CUtensorMap& mW1k, const CUtensorMap& mW3k,
                            const CUtensorMap& mDG, const CUtensorMap& mDU, const PlanPtrs& pl,
                            int P, int H, int F, int E, const EpiAux& aux,
-                           __nv_bfloat16* dx_perm, int* status, cudaStream_t s) {
+                           __nv_bfloat16* dx_perm, int* status, cudaStream_t s,
+                           StreamK sk = StreamK{nullptr, nullptr}) {
   const long long nb_max = max_blocks(P, E, kBN);
   constexpr int kAF = kPairF ? 2 : 1, kBufF = kPairF ? 1 : 2;
   constexpr int kAH = kPairH ? 2 : 1, kBufH = kPairH ? 1 : 2;
@@ -856,7 +857,7 @@ cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
   // dx_perm = dg W1[e]^T + du W3[e]^T (M = H, K = F in two phases)
   return launch_gemm<kAH, kEpiBf16, kBN, kBufH, true, true>(
       mW1k, mW3k, mDG, mDU, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
-      nb_max, dx_perm, H, EpiAux{}, ox, status, s);
+      nb_max, dx_perm, H, EpiAux{}, ox, status, s, sk);
 }
 
 }  // namespace
@@ -912,8 +913,9 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
                          const int32_t* block_off, const int32_t* num_blocks,
                          const int32_t* block_expert, int P, int H, int F, int E,
                          __nv_bfloat16* dg, __nv_bfloat16* du, __nv_bfloat16* dx_perm,
-                         int* status, cudaStream_t s) {
+                         int* status, cudaStream_t s, const StreamKSpace* sks) {
   if (P == 0) return cudaSuccess;
+  const StreamK sk = sks ? StreamK{sks->part, sks->cnt} : StreamK{nullptr, nullptr};
   CUtensorMap mW2k, mW1k, mW3k, mDY, mDG, mDU;
   if (!map_weights_k(&mW2k, W2, F, H, E) || !map_weights_k(&mW1k, W1, H, F, E) ||
       !map_weights_k(&mW3k, W3, H, F, E) || !map_rows(&mDY, dY, H, P) ||
@@ -924,10 +926,10 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
   switch (ffn_mode(P, E)) {
     case FfnMode::kTiny:
       return launch_dgrad_t<kBlockRowsTiny, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P,
-                                                          H, F, E, aux, dx_perm, status, s);
+                                                          H, F, E, aux, dx_perm, status, s, sk);
     case FfnMode::kSmall:
       return launch_dgrad_t<kBlockRows, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl, P, H,
-                                                      F, E, aux, dx_perm, status, s);
+                                                      F, E, aux, dx_perm, status, s, sk);
     default: {
       const bool pf = F % (2 * BM) == 0, ph = H % (2 * BM) == 0;
       if (pf && ph)

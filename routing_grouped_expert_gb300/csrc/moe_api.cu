@@ -478,7 +478,9 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
   __nv_bfloat16* dg = ws_ptr<__nv_bfloat16>(ws, R.dg);
   __nv_bfloat16* du = ws_ptr<__nv_bfloat16>(ws, R.du);
   const auto* dout_b = static_cast<const __nv_bfloat16*>(dout);
-  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
+  // the status word and the split counters of DGrad dx (adjacent) start at zero
+  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
   MOE_TRY(launch_scale_gather(dout_b, sorted_src, topk_w, P, H, k, dY, s));
   MOE_TRY(launch_dw_dlogits(dout_b, y, dest_of, topk_idx, router_logits, T, H, E, k, dlogits, s));
   MOE_TRY(launch_dgrad(dY, ws_ptr<__nv_bfloat16>(ws, R.g), ws_ptr<__nv_bfloat16>(ws, R.u),
@@ -487,7 +489,7 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
                        static_cast<const __nv_bfloat16*>(W2), offsets,
                        ws_ptr<int32_t>(ws, L.block_off), ws_ptr<int32_t>(ws, L.num_blocks),
                        ws_ptr<int32_t>(ws, L.block_expert), P, H, F, E, dg, du, dx_perm, status,
-                       s));
+                       s, &sks));
   MOE_TRY(launch_combine(dx_perm, dest_of, nullptr, T, H, k, static_cast<__nv_bfloat16*>(dx), s));
   MOE_TRY(launch_wgrad(x_perm, h, dY, dg, du, offsets, P, H, F, E,
                        static_cast<__nv_bfloat16*>(dW1), static_cast<__nv_bfloat16*>(dW3),

@@ -270,7 +270,7 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
                          const int32_t* block_off, const int32_t* num_blocks,
                          const int32_t* block_expert, int P, int H, int F, int E,
                          __nv_bfloat16* dg, __nv_bfloat16* du, __nv_bfloat16* dx_perm,
-                         int* status, cudaStream_t s);
+                         int* status, cudaStream_t s, const StreamKSpace* sks = nullptr);
 // out[t] = sum_j w[t,j] y_sorted[dest_of[t*k+j]] (+ y_shared[t] when given)
 cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,

@@ -34,6 +34,7 @@ CASES = {  # name: (T, H, F, E, k) -- block mode from the mean rows per expert
     "many_empty_experts": (20, 128, 256, 32, 1),
     "fine_grained_like": (150, 256, 128, 32, 6),
     "max_experts_topk": (64, 128, 128, 1024, 32),      # the header's limits
+    "split_dx_tiny": (64, 2560, 256, 16, 2),          # 320 dx tiles: balanced K split
 }
 
 
