@@ -23,8 +23,8 @@
  *     except moe_get_device_status.
  *   - `ws` is a caller-owned device workspace of at least
  *     moe_workspace_size(T, H, F, E, k) bytes, 256-byte aligned.  It holds
- *     the intermediates (gathered rows, expert activations and outputs), a
- *     fixed 32 MiB of partial tiles for the balanced K split of FC2, and a
+ *     the intermediates (gathered rows, expert activations and outputs),
+ *     8 to 32 MiB of partial tiles for the balanced K split of FC2, and a
  *     device status word.  Its contents need no initialisation.  Calls that
  *     share one workspace must not overlap in time (use one stream per
  *     workspace).

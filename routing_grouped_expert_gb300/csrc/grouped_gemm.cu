@@ -169,38 +169,45 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
 // does not depend on which CTA finishes) and stores the tile.  Nothing waits
 // on another CTA.
 struct StreamK {
-  float* part;   // [CTAs][2][kTileM][kBN]: slot 0 the CTA's first part, 1 its last
+  float* part;   // [CTAs][2] slots of [kNumA][kTileM][kBN]: 0 the CTA's first part, 1 its last
   int* cnt;      // [CTAs] arrivals at each CTA boundary, zero between launches
+  size_t slot_bytes;   // capacity of one slot
 };
 
-// The (tile, K-stage range) segments a CTA processes, in order.
+// The (tile, K-stage range) segments a CTA processes, in order.  Whole tiles
+// are taken round-robin (CTA c: tiles c, c + G, ...), so the CTAs running side
+// by side work on neighbouring tiles, which share weight rows and token blocks
+// in L2 and DRAM pages.  With a balanced split, the last one to two rounds'
+// worth of tiles (between G and 2G of them) are instead cut into equal
+// contiguous K ranges, one per CTA; each range is at least one tile long, so a
+// tile is cut between at most two neighbouring CTAs.
 struct Segments {
-  long long u, end;   // stream-K: this CTA's range of (tile, stage) units
-  int w, step, total, nkb;
+  long long u, end;   // the CTA's range of (tile, stage) units in the split tail
+  int w, step, nkb, round_robin_end;
   bool sk;
-  __device__ Segments(bool split_ok, int total_, int nkb_)
-      : w(blockIdx.x), step(gridDim.x), total(total_), nkb(nkb_) {
-    sk = split_ok && total > (int)gridDim.x && total % (int)gridDim.x != 0;
-    // (measured: ranges cut at any K stage balance best; rounding the cuts to
-    // 1/16 .. 1/4 of a tile was slower)
-    const long long U = (long long)total * nkb;
-    u = U * blockIdx.x / gridDim.x;
-    end = U * (blockIdx.x + 1) / gridDim.x;
+  __device__ Segments(bool split_ok, int total, int nkb_)
+      : w(blockIdx.x), step(gridDim.x), nkb(nkb_) {
+    const int G = gridDim.x;
+    sk = split_ok && total > G && total % G != 0;
+    round_robin_end = sk ? (total / G - 1) * G : total;
+    const long long base = (long long)round_robin_end * nkb;
+    const long long U = (long long)(total - round_robin_end) * nkb;
+    u = base + U * blockIdx.x / G;
+    end = base + U * (blockIdx.x + 1) / G;
   }
   __device__ bool next(int& wo, int& kb0, int& kb1) {
-    if (sk) {
-      if (u >= end) return false;
-      wo = (int)(u / nkb);
-      kb0 = (int)(u - (long long)wo * nkb);
-      kb1 = (int)min((long long)nkb, kb0 + (end - u));
-      u += kb1 - kb0;
+    if (w < round_robin_end) {
+      wo = w;
+      kb0 = 0;
+      kb1 = nkb;
+      w += step;
       return true;
     }
-    if (w >= total) return false;
-    wo = w;
-    kb0 = 0;
-    kb1 = nkb;
-    w += step;
+    if (!sk || u >= end) return false;
+    wo = (int)(u / nkb);
+    kb0 = (int)(u - (long long)wo * nkb);
+    kb1 = (int)min((long long)nkb, kb0 + (end - u));
+    u += kb1 - kb0;
     return true;
   }
 };
@@ -252,9 +259,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = *num_blocks_ptr * n_mt;
-  // stream-K only for a single weight tile with two accumulator buffers and a
-  // bf16 output (FC2 and DGrad dx of small token blocks)
+  // The balanced split for one weight tile with two accumulator buffers and a
+  // bf16 output (FC2 and DGrad dx of small token blocks).  Measured elsewhere
+  // it loses: with one accumulator buffer the cut tiles' partial stores stall
+  // the next tile's MMAs, and FC1 prefers every CTA on neighbouring tiles.
   constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2;
+  constexpr size_t kSlot = (size_t)kNumA * BM * kBN;   // floats of one partial tile
   const bool sk_ok = kSKCapable && sk.part != nullptr;
   const int nkb = K / BK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
@@ -482,20 +492,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         if (kb0 > 0 || kb1 < nkb_all) {
           const bool head = kb0 == 0;   // the tile's first stages: this CTA's last part
           const int c = blockIdx.x;
-          float* mine = sk.part + ((size_t)c * 2 + (head ? 1 : 0)) * BM * kBN;
+          float* mine = sk.part + ((size_t)c * 2 + (head ? 1 : 0)) * kSlot;
           const float* theirs =
-              sk.part + (head ? (size_t)(c + 1) * 2 : (size_t)(c - 1) * 2 + 1) * BM * kBN;
+              sk.part + (head ? (size_t)(c + 1) * 2 : (size_t)(c - 1) * 2 + 1) * kSlot;
           int* cnt = sk.cnt + (head ? c : c - 1);
-          for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tb + c0, v);
-            tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(mine + (size_t)(q * 32 + lane) * kBN + c0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-          }
+          for (int a = 0; a < kNumA; ++a)
+            for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(tb + a * kBN + c0, v);
+              tmem_ld_wait();
+              float4* dst = reinterpret_cast<float4*>(
+                  mine + ((size_t)a * BM + q * 32 + lane) * kBN + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]),
+                                     __uint_as_float(v[4 * j + 3]));
+            }
           __threadfence();   // this thread's partial is visible device-wide
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->sk_written);
@@ -548,15 +562,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         tmem_ld_wait();
         if constexpr (kSKCapable) {
           if (other != nullptr) {   // finish a cut tile: add the neighbour's part
-            const float4* o4 =
-                reinterpret_cast<const float4*>(other + (size_t)(q * 32 + lane) * kBN + c0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float4 t = __ldcg(o4 + j);
-              g[4 * j] = __float_as_uint(__uint_as_float(g[4 * j]) + t.x);
-              g[4 * j + 1] = __float_as_uint(__uint_as_float(g[4 * j + 1]) + t.y);
-              g[4 * j + 2] = __float_as_uint(__uint_as_float(g[4 * j + 2]) + t.z);
-              g[4 * j + 3] = __float_as_uint(__uint_as_float(g[4 * j + 3]) + t.w);
+            for (int a = 0; a < kNumA; ++a) {
+              uint32_t* r = a == 0 ? g : g2;
+              const float4* o4 = reinterpret_cast<const float4*>(
+                  other + ((size_t)a * BM + q * 32 + lane) * kBN + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float4 t = __ldcg(o4 + j);
+                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + t.x);
+                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + t.y);
+                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + t.z);
+                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + t.w);
+              }
             }
           }
         }
@@ -651,7 +669,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         // hand each 64-column group back as soon as this warp has read it
         for (int r = 0; r < C::kRegions; ++r) {
           for (int c0 = 64 * r + 16 * half; c0 < 64 * r + 64; c0 += 32)
-            if (c0 < it.nrows) chunk(c0);
+            if (store && c0 < it.nrows) chunk(c0);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->acc_region[r]);
@@ -745,7 +763,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
                         const OutMaps& outs, int* status, cudaStream_t s,
-                        StreamK sk = StreamK{nullptr, nullptr}) {
+                        StreamK sk = StreamK{nullptr, nullptr, 0}) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   cudaError_t err =
@@ -756,7 +774,8 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   const int n_mt = (M_total + C::kFeatPerItem - 1) / C::kFeatPerItem;
   const long long items = nb_max * n_mt;
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  if (grid > kStreamKMaxCtas) sk = StreamK{nullptr, nullptr};
+  if (grid > kStreamKMaxCtas || (size_t)kNumA * BM * kBN * 4 > sk.slot_bytes)
+    sk = StreamK{nullptr, nullptr, 0};
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, b1, offsets, block_off, num_blocks,
                                              block_expert, n_mt, K, out, ld_out, M_total, aux,
                                              outs, sk, status);
@@ -804,7 +823,7 @@ bool map_rows(CUtensorMap* m, const void* X, int K, int P) {
 template <int kBN, int kBufs1>
 cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUtensorMap& mX,
                        const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
-                       const EpiAux* save, int* status, cudaStream_t s) {
+                       const EpiAux* save, int* status, cudaStream_t s, StreamK sk) {
   const long long nb_max = max_blocks(P, E, kBN);
   OutMaps om;
   if (!map_out(&om.m[0], h, F, P)) return cudaErrorInvalidValue;
@@ -813,17 +832,17 @@ cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUt
       return cudaErrorInvalidValue;
     return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
                                                        pl.num_blocks, pl.block_expert, F, H,
-                                                       nb_max, h, F, *save, om, status, s);
+                                                       nb_max, h, F, *save, om, status, s, sk);
   }
   return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
                                                  pl.num_blocks, pl.block_expert, F, H, nb_max, h,
-                                                 F, EpiAux{}, om, status, s);
+                                                 F, EpiAux{}, om, status, s, sk);
 }
 
 template <int kNumA, int kBN, int kBufs>
 cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const PlanPtrs& pl, int P,
                        int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s,
-                       StreamK sk = StreamK{nullptr, nullptr}) {
+                       StreamK sk = StreamK{nullptr, nullptr, 0}) {
   OutMaps om;
   if (!map_out(&om.m[0], y, H, P)) return cudaErrorInvalidValue;
   return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(mW2, mW2, mH, mH, pl.offsets, pl.block_off,
@@ -841,7 +860,7 @@ cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
                            const CUtensorMap& mDG, const CUtensorMap& mDU, const PlanPtrs& pl,
                            int P, int H, int F, int E, const EpiAux& aux,
                            __nv_bfloat16* dx_perm, int* status, cudaStream_t s,
-                           StreamK sk = StreamK{nullptr, nullptr}) {
+                           StreamK sk = StreamK{nullptr, nullptr, 0}) {
   const long long nb_max = max_blocks(P, E, kBN);
   constexpr int kAF = kPairF ? 2 : 1, kBufF = kPairF ? 1 : 2;
   constexpr int kAH = kPairH ? 2 : 1, kBufH = kPairH ? 1 : 2;
@@ -852,7 +871,7 @@ cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
     return cudaErrorInvalidValue;
   cudaError_t err = launch_gemm<kAF, kEpiSwigluBwd, kBN, kBufF, true>(
       mW2k, mW2k, mDY, mDY, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H,
-      nb_max, nullptr, 0, aux, oh, status, s);
+      nb_max, nullptr, 0, aux, oh, status, s, sk);
   if (err != cudaSuccess) return err;
   // dx_perm = dg W1[e]^T + du W3[e]^T (M = H, K = F in two phases)
   return launch_gemm<kAH, kEpiBf16, kBN, kBufH, true, true>(
@@ -887,24 +906,25 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
     return cudaErrorInvalidValue;
   const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
   const FfnMode mode = ffn_mode(P, E);
+  // balanced K split when the tiles do not fill the SMs evenly
+  const StreamK sk =
+      sks ? StreamK{sks->part, sks->cnt, sks->slot_bytes} : StreamK{nullptr, nullptr, 0};
   cudaError_t err;
   if (mode == FfnMode::kTiny)
-    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
+    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
   else if (mode == FfnMode::kSmall)
-    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
+    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
   else
-    err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s);
+    err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
-  // FC2 of small blocks: balanced K split when its tiles do not fill the SMs evenly
-  const StreamK sk = sks ? StreamK{sks->part, sks->cnt} : StreamK{nullptr, nullptr};
   if (mode == FfnMode::kTiny)
     return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   if (mode == FfnMode::kSmall)
     return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   if (fc2_paired(H, F))
-    return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s);
-  return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s);
+    return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
+  return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
 }
 
 cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,
@@ -915,7 +935,8 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
                          __nv_bfloat16* dg, __nv_bfloat16* du, __nv_bfloat16* dx_perm,
                          int* status, cudaStream_t s, const StreamKSpace* sks) {
   if (P == 0) return cudaSuccess;
-  const StreamK sk = sks ? StreamK{sks->part, sks->cnt} : StreamK{nullptr, nullptr};
+  const StreamK sk =
+      sks ? StreamK{sks->part, sks->cnt, sks->slot_bytes} : StreamK{nullptr, nullptr, 0};
   CUtensorMap mW2k, mW1k, mW3k, mDY, mDG, mDU;
   if (!map_weights_k(&mW2k, W2, F, H, E) || !map_weights_k(&mW1k, W1, H, F, E) ||
       !map_weights_k(&mW3k, W3, H, F, E) || !map_rows(&mDY, dY, H, P) ||
@@ -934,15 +955,15 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
       const bool pf = F % (2 * BM) == 0, ph = H % (2 * BM) == 0;
       if (pf && ph)
         return launch_dgrad_t<kBlockRowsLarge, true, true>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
-                                                           P, H, F, E, aux, dx_perm, status, s);
+                                                           P, H, F, E, aux, dx_perm, status, s, sk);
       if (pf)
         return launch_dgrad_t<kBlockRowsLarge, true, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
-                                                            P, H, F, E, aux, dx_perm, status, s);
+                                                            P, H, F, E, aux, dx_perm, status, s, sk);
       if (ph)
         return launch_dgrad_t<kBlockRowsLarge, false, true>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
-                                                            P, H, F, E, aux, dx_perm, status, s);
+                                                            P, H, F, E, aux, dx_perm, status, s, sk);
       return launch_dgrad_t<kBlockRowsLarge, false, false>(mW2k, mDY, mW1k, mW3k, mDG, mDU, pl,
-                                                           P, H, F, E, aux, dx_perm, status, s);
+                                                           P, H, F, E, aux, dx_perm, status, s, sk);
     }
   }
 }

@@ -139,7 +139,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s,
                         pdl));
   MOE_TRY(mark(4));
-  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
@@ -151,7 +151,7 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                                static_cast<const __nv_bfloat16*>(sh->W1),
                                static_cast<const __nv_bfloat16*>(sh->W3),
                                static_cast<const __nv_bfloat16*>(sh->W2), T, H, sh->Fs, 1, sh->h,
-                               sh->y, status, s, nullptr, nullptr, &sks));
+                               sh->y, status, s));   // its block size differs: no split
   MOE_TRY(mark(6));
   MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
                          sh ? sh->y : nullptr, pdl));
@@ -231,7 +231,7 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
   int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
   __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
-  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and FC2's split counters (adjacent) start at zero
   MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
   MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert,
@@ -478,7 +478,7 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
   __nv_bfloat16* dg = ws_ptr<__nv_bfloat16>(ws, R.dg);
   __nv_bfloat16* du = ws_ptr<__nv_bfloat16>(ws, R.du);
   const auto* dout_b = static_cast<const __nv_bfloat16*>(dout);
-  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt)};
+  const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and the split counters of DGrad dx (adjacent) start at zero
   MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
   MOE_TRY(launch_scale_gather(dout_b, sorted_src, topk_w, P, H, k, dY, s));

@@ -48,6 +48,13 @@ inline FfnMode ffn_mode(long long P, int E) {
   if (P <= (long long)kSmallModeMeanRows * E) return FfnMode::kSmall;
   return FfnMode::kLarge;
 }
+inline int ffn_block_rows_of(long long P, int E) {
+  switch (ffn_mode(P, E)) {
+    case FfnMode::kTiny: return kBlockRowsTiny;
+    case FfnMode::kSmall: return kBlockRows;
+    default: return kBlockRowsLarge;
+  }
+}
 // Permute chunking: one CTA handles the assignments of kChunkAssign / k
 // consecutive tokens (at most kChunkAssign assignments).
 constexpr int kChunkAssign = 512;
@@ -88,7 +95,8 @@ struct WsLayout {
   size_t x_perm;        // bf16[P*H]
   size_t h;             // bf16[P*F]
   size_t y;             // bf16[P*H]
-  size_t sk_part;       // f32[kStreamKMaxCtas*2*kTileM*kBlockRows]   FC2 split partials
+  size_t sk_part;       // f32 [kStreamKMaxCtas][2] slots of sk_slot bytes: split partials
+  size_t sk_slot;       // bytes of one slot: a 128-row accumulator of the layer's block size
   size_t stage_x;       // bf16[T*H]   device staging for moe_forward_host
   size_t stage_logits;  // f32[T*E]
   size_t stage_out;     // bf16[T*H]
@@ -144,7 +152,8 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   L.x_perm = take(P * H * 2);
   L.h = take(P * F * 2);
   L.y = take(P * H * 2);
-  L.sk_part = take((size_t)kStreamKMaxCtas * 2 * kTileM * kBlockRows * 4);
+  L.sk_slot = (size_t)kTileM * ffn_block_rows_of(P, E) * 4;
+  L.sk_part = take((size_t)kStreamKMaxCtas * 2 * L.sk_slot);
   L.stage_x = take((size_t)T * H * 2);   // the host-buffer staging comes last
   L.stage_logits = take((size_t)T * E * 4);
   L.stage_out = take((size_t)T * H * 2);
@@ -249,8 +258,9 @@ struct EpiAux {
 // Scratch of FC2's balanced K split: partial tiles and boundary counters.  The
 // counters must be zero before a launch; every launch leaves them zero.
 struct StreamKSpace {
-  float* part;   // [kStreamKMaxCtas][2][kTileM][kBlockRows] fp32
-  int* cnt;      // [kStreamKMaxCtas]
+  float* part;         // [kStreamKMaxCtas][2] slots of slot_bytes (fp32 partial tiles)
+  int* cnt;            // [kStreamKMaxCtas]
+  size_t slot_bytes;
 };
 // FC1 (+SwiGLU) and FC2 over the expert groups.  With `save`, FC1 also keeps
 // its pre-activations g = x W1, u = x W3 (bf16, [P, F]) for the backward.
