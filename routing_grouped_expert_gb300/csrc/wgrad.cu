@@ -14,9 +14,10 @@
 // are row-major [P, *] buffers read as MN-major tensor-core operands by TMA
 // boxes of 64 rows x 64 columns.  The
 // last stage of an expert usually runs past its rows into the next expert's:
-// before the MMAs the MMA warp zeroes those rows in shared memory (whole
-// 128-byte rows, so the swizzle does not matter), then fences them for the
-// tensor core.  Experts without rows get zero gradients.
+// its MMAs stop at the last 16-row K group holding rows of the expert, and
+// the MMA warp zeroes the rest of that group in shared memory (whole 128-byte
+// rows, so the swizzle does not matter), then fences it for the tensor core.
+// Experts without rows get zero gradients.
 //
 // Warp roles as in the forward engine: warp 0 TMA producer, warp 1 MMA
 // (all lanes help zero the tail; lane 0 issues), warps 2-9 epilogue.  The
@@ -39,15 +40,22 @@ constexpr int BM = kTileM;            // dW rows per MMA
 constexpr int BK = 64;                // routed rows per stage
 constexpr int kBox = 64 * BK * 2;     // one 64-column x 64-row box: 8 KB
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kSmemBudget = 196608;   // operand ring
-constexpr int kStgBytes = 32 * 64 * 2; // epilogue staging per warp: 32 rows x 64 columns
+constexpr int kZeroWarp = 2 + kEpiWarps;   // clears the rows of a stage past its expert
+constexpr int kThreads = 32 * (kZeroWarp + 1);
+// Epilogue staging buffers per warp (each 32 rows x 64 columns); with more
+// than one, a warp converts its next chunk while earlier stores still read.
+#ifndef MOE_WGRAD_STG_BUFS
+#define MOE_WGRAD_STG_BUFS 1
+#endif
+constexpr int kStgBufs = MOE_WGRAD_STG_BUFS;
+constexpr int kStgBytes = 32 * 64 * 2;
+constexpr int kSmemBudget = kStgBufs == 1 ? 196608 : 163840;   // operand ring
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-template <int kNumB, bool kPairM>
+template <int kNumB, bool kPairM, int kBN_>
 struct WCfg {
-  static constexpr int kMS = kPairM ? 2 : 1;                      // 128-row A sub-tiles
-  static constexpr int kBN = (kPairM && kNumB == 1) ? 256 : 128;  // columns per B operand
+  static constexpr int kMS = kPairM ? 2 : 1;   // 128-row A sub-tiles
+  static constexpr int kBN = kBN_;             // columns per B operand
   static constexpr int kTileRows = kMS * BM;
   static constexpr int kABytes = kMS * 2 * kBox;
   static constexpr int kBBytes = (kBN / 64) * kBox;
@@ -59,14 +67,16 @@ struct WCfg {
   static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kStgOffset = kBarOffset + 1024;              // 1 KB-aligned for the swizzle
-  static constexpr int kSmemBytes = kStgOffset + kEpiWarps * kStgBytes + 1024;
+  static constexpr int kSmemBytes = kStgOffset + kEpiWarps * kStgBufs * kStgBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kStages >= 2 && kStages <= 8, "stages");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+  static_assert(kBN == 128 || kBN == 256, "B tile width");
 };
 
 struct WBars {
   uint64_t full[8];
+  uint64_t ready[8];   // a stage's data landed and its rows past the expert are cleared
   uint64_t empty[8];
   uint64_t acc_full[2];
   uint64_t acc_empty[2][4];   // per buffer, per 128-column group
@@ -110,9 +120,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Until every committed store of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Until at most kPending committed stores of this thread still read shared memory.
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
 }
 // Until every committed store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
@@ -123,13 +134,13 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int kNumB, bool kPairM>
+template <int kNumB, bool kPairM, int kBN_>
 __global__ void __launch_bounds__(kThreads, 1)
 wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
              const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
              const __grid_constant__ CUtensorMap tmO1, const int32_t* __restrict__ offsets,
              int E, int M_total, int N_total, int* __restrict__ status) {
-  using C = WCfg<kNumB, kPairM>;
+  using C = WCfg<kNumB, kPairM, kBN_>;
   constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -142,6 +153,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->ready[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
@@ -186,17 +198,12 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           uint64_t* fb = &bars->full[stage];
           const int r = it.row0 + kb * BK;
           mbar_arrive_expect_tx(fb, C::kStageBytes);
+          // one box per operand: all its 64-column atoms, 64 rows each
+          tma_load_3d(sA, &tmA, fb, 0, r, it.m0 / 64, pol);
 #pragma unroll
-          for (int bx = 0; bx < 2 * C::kMS; ++bx)
-            tma_load_2d(sA + bx * kBox, &tmA, fb, it.m0 + 64 * bx, r, pol);
-#pragma unroll
-          for (int b = 0; b < kNumB; ++b) {
-            const CUtensorMap* mb = b == 0 ? &tmB0 : &tmB1;
-            uint8_t* sB = sA + C::kABytes + b * C::kBBytes;
-#pragma unroll
-            for (int bx = 0; bx < kBN / 64; ++bx)
-              tma_load_2d(sB + bx * kBox, mb, fb, it.n0 + 64 * bx, r, pol);
-          }
+          for (int b = 0; b < kNumB; ++b)
+            tma_load_3d(sA + C::kABytes + b * C::kBBytes, b == 0 ? &tmB0 : &tmB1, fb, 0, r,
+                        it.n0 / 64, pol);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -236,23 +243,13 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       const uint32_t d0 = tmem_base + (uint32_t)(acc * C::kAccCols);
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs))) {
+                        mbar_wait(&bars->ready[stage], phase, abort_flag, kWaitLimitNs))) {
           ok = false;
           break;
         }
+        // the MMAs cover only the 16-row K groups holding rows of the expert
         const int valid = it.rows - kb * BK;     // rows of this expert in the stage
-        if (valid < BK) {
-          // zero rows [valid, 64) of every 64-row box of the stage
-          uint4* base = reinterpret_cast<uint4*>(smem + stage * C::kStageBytes);
-          const int per_box = (BK - valid) * 8;  // 16-byte chunks to clear per box
-          const int nbox = C::kStageBytes / kBox;
-          for (int i = lane; i < nbox * per_box; i += 32) {
-            const int bx = i / per_box, j = i - bx * per_box;
-            base[bx * (kBox / 16) + valid * 8 + j] = make_uint4(0, 0, 0, 0);
-          }
-          fence_async_smem();
-        }
-        __syncwarp();
+        const int nkk = valid >= BK ? BK / 16 : (valid + 15) >> 4;
         tc_fence_after();
         const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
         if (kb == 0) {
@@ -267,6 +264,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             if (lane == 0) {
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk) {
+                if (kk >= nkk) break;
                 const uint64_t da = sdesc_sw128(a0 + ms * 2 * kBox + kk * 2048, kBox, 1024);
                 const uint64_t db =
                     sdesc_sw128(a0 + C::kABytes + b * C::kBBytes + kk * 2048, kBox, 1024);
@@ -280,6 +278,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         } else if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nkk) break;
             // both operands MN-major: 64-wide atoms 8 KB apart, 8-row groups 1 KB
             // apart, K step of 16 rows = 2 KB
 #pragma unroll
@@ -318,11 +317,53 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       if (!mbar_wait(&bars->drain, 0, nullptr, kWaitLimitNs))
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailDrain);
     }
+  } else if (warp == kZeroWarp) {
+    // ------------------------------------------------- tail rows of a stage
+    // The last stage of an expert's tile ends inside a 16-row K group or
+    // runs past it: rows past the expert in the last group the MMAs read (the
+    // next expert's, or the zero fill past the end) are cleared in every box
+    // of the stage (whole 128-byte rows, so the swizzle does not matter) and
+    // fenced for the tensor core before the stage is handed to the MMA warp.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const WItem it = decode_witem<C::kTileRows, kBN>(w, n_m, n_n, offsets);
+      const int nkb = (it.rows + BK - 1) / BK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bars->full[stage], phase, abort_flag, kWaitLimitNs))) {
+          ok = false;
+          break;
+        }
+        const int valid = it.rows - kb * BK;
+        const int pad = (((valid + 15) >> 4) << 4) - valid;   // 0..15 when valid < BK
+        if (valid < BK && pad > 0) {
+          uint4* base = reinterpret_cast<uint4*>(smem + stage * C::kStageBytes) + valid * 8;
+#pragma unroll
+          for (int bx = 0; bx < C::kStageBytes / kBox; ++bx)
+            for (int i = lane; i < pad * 8; i += 32)
+              base[bx * (kBox / 16) + i] = make_uint4(0, 0, 0, 0);
+          fence_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ready[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      set_status(status, MOE_ERR_TIMEOUT, kWaitDetailMma);
+      *abort_flag = 1;
+    }
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;  // which alternate 64-column chunks it takes
-    uint8_t* stg = smem + C::kStgOffset + (warp - 2) * kStgBytes;
+    uint8_t* stg0 = smem + C::kStgOffset + (warp - 2) * kStgBufs * kStgBytes;
+    int nstg = 0;   // chunks staged by this warp so far
     const uint64_t pol_out = policy_evict_first();   // written once, not read here
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -336,46 +377,58 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      // The warp's chunks of the tile: chunk i is accumulator t = i / kCPT,
+      // columns 64 * half + 128 * (i % kCPT), i.e. the warp's part of
+      // 128-column group i.  Chunk i + 1 is read from TMEM and its group
+      // handed back before chunk i is converted and stored, so the next tile's
+      // MMAs wait for the drain one chunk less.
+      constexpr int kCPT = kBN / 128;
+      constexpr int kNC = C::kMS * kNumB * kCPT;
+      uint32_t v[2][64];
+      auto read_chunk = [&](int i, uint32_t* dst) {
+        if (it.rows > 0) {
 #pragma unroll
-      for (int t = 0; t < C::kMS * kNumB; ++t) {
-        const int ms = t / kNumB, b = t % kNumB;
+          for (int j = 0; j < 4; ++j)
+            tmem_ld_32x32b_x16(tb + (i / kCPT) * kBN + 64 * half + 128 * (i % kCPT) + 16 * j,
+                               *reinterpret_cast<uint32_t(*)[16]>(dst + 16 * j));
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) dst[c] = 0u;
+        }
+        // this warp's part of the 128-column group is read: hand it back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->acc_empty[acc][i]);
+      };
+      read_chunk(0, v[0]);
+#pragma unroll
+      for (int i = 0; i < kNC; ++i) {
+        if (i + 1 < kNC) read_chunk(i + 1, v[(i + 1) & 1]);
+        const uint32_t* src = v[i & 1];
+        const int t = i / kCPT, ms = t / kNumB, b = t % kNumB;
         const int orow = it.e * M_total + it.m0 + ms * BM + q * 32;   // the warp's first row
+        // the store that last used this buffer has read it
+        if (lane == 0) bulk_wait_read<kStgBufs - 1>();
+        __syncwarp();
+        uint8_t* stg = stg0 + (nstg++ % kStgBufs) * kStgBytes;
+        // row `lane` of the box: 16-byte chunk j sits at j ^ (row & 7) (128B swizzle)
 #pragma unroll
-        for (int c0 = 64 * half; c0 < kBN; c0 += 128) {
-          uint32_t v[64];
-          if (it.rows > 0) {
+        for (int j = 0; j < 8; ++j) {
+          uint4 pk;
+          __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tmem_ld_32x32b_x16(tb + t * kBN + c0 + 16 * i,
-                                 *reinterpret_cast<uint32_t(*)[16]>(&v[16 * i]));
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) v[c] = 0u;
-          }
-          // this warp's part of the 128-column group is read: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->acc_empty[acc][t * (kBN / 128) + c0 / 128]);
-          if (lane == 0) bulk_wait_read_all();   // the previous store has left the buffer
-          __syncwarp();
-          // row `lane` of the box: 16-byte chunk j sits at j ^ (row & 7) (128B swizzle)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 pk;
-            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              p2[c] = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * c]),
-                                            __uint_as_float(v[8 * j + 2 * c + 1]));
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(b == 0 ? &tmO0 : &tmO1, stg, it.n0 + c0, orow, pol_out);
-            bulk_commit();
-          }
+          for (int c = 0; c < 4; ++c)
+            p2[c] = __floats2bfloat162_rn(__uint_as_float(src[8 * j + 2 * c]),
+                                          __uint_as_float(src[8 * j + 2 * c + 1]));
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(b == 0 ? &tmO0 : &tmO1, stg, it.n0 + 64 * half + 128 * (i % kCPT), orow,
+                       pol_out);
+          bulk_commit();
         }
       }
       if (++acc == C::kAccBufs) {
@@ -400,12 +453,15 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   }
 }
 
-// Row-major [P, cols] buffer as MN-major operand boxes of 64 columns x 64 rows.
-bool map_rows64(CUtensorMap* m, const void* X, int cols, int P) {
-  const cuuint64_t d[2] = {(cuuint64_t)cols, (cuuint64_t)P};
-  const cuuint64_t st[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)BK};
-  return make_tensor_map_bf16(m, X, 2, reinterpret_cast<const unsigned long long*>(d),
+// Row-major [P, cols] buffer as MN-major operand boxes of `atoms` 64-column
+// atoms x 64 rows: a 3-D view (64 columns, rows, atoms) whose box lands in
+// shared memory atom by atom, each atom 64 rows of 128 bytes, as the
+// tensor-core descriptors expect; one TMA instruction moves the whole box.
+bool map_rows64(CUtensorMap* m, const void* X, int cols, int P, int atoms) {
+  const cuuint64_t d[3] = {64, (cuuint64_t)P, (cuuint64_t)cols / 64};
+  const cuuint64_t st[2] = {(cuuint64_t)cols * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)BK, (cuuint32_t)atoms};
+  return make_tensor_map_bf16(m, X, 3, reinterpret_cast<const unsigned long long*>(d),
                               reinterpret_cast<const unsigned long long*>(st),
                               reinterpret_cast<const unsigned int*>(box));
 }
@@ -421,25 +477,34 @@ bool map_grad_out(CUtensorMap* m, const void* W, int E, int M, int N) {
                               reinterpret_cast<const unsigned int*>(box));
 }
 
-template <int kNumB, bool kPairM>
-cudaError_t launch_w(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                     const int32_t* offsets, int E, int M_total, int N_total, __nv_bfloat16* o0,
-                     __nv_bfloat16* o1, int* status, cudaStream_t s) {
-  using C = WCfg<kNumB, kPairM>;
-  CUtensorMap mo0, mo1;
-  if (!map_grad_out(&mo0, o0, E, M_total, N_total) || !map_grad_out(&mo1, o1, E, M_total, N_total))
+template <int kNumB, bool kPairM, int kBN>
+cudaError_t launch_w(const __nv_bfloat16* A, int a_cols, const __nv_bfloat16* B0,
+                     const __nv_bfloat16* B1, int b_cols, int P, const int32_t* offsets, int E,
+                     __nv_bfloat16* o0, __nv_bfloat16* o1, int* status, cudaStream_t s) {
+  using C = WCfg<kNumB, kPairM, kBN>;
+  const int M_total = a_cols, N_total = b_cols;
+  CUtensorMap ma, mb0, mb1, mo0, mo1;
+  if (!map_rows64(&ma, A, a_cols, P, 2 * C::kMS) || !map_rows64(&mb0, B0, b_cols, P, kBN / 64) ||
+      !map_rows64(&mb1, B1, b_cols, P, kBN / 64) ||
+      !map_grad_out(&mo0, o0, E, M_total, N_total) || !map_grad_out(&mo1, o1, E, M_total, N_total))
     return cudaErrorInvalidValue;
-  auto kern = wgrad_kernel<kNumB, kPairM>;
+  auto kern = wgrad_kernel<kNumB, kPairM, kBN>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long items = (long long)E * (M_total / C::kTileRows) * (N_total / C::kBN);
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, mo0, mo1, offsets, E, M_total, N_total,
-                                             status);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(ma, mb0, mb1, mo0, mo1, offsets, E, M_total,
+                                             N_total, status);
   return cudaGetLastError();
 }
 
+
+// Wide tiles up to this many routed rows per expert on average.
+#ifndef MOE_WGRAD_WIDE_MAX_ROWS
+#define MOE_WGRAD_WIDE_MAX_ROWS 64
+#endif
+bool wgrad_wide(int P, int E) { return (long long)P <= (long long)MOE_WGRAD_WIDE_MAX_ROWS * E; }
 
 }  // namespace
 
@@ -449,20 +514,28 @@ cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
                          int E, __nv_bfloat16* dW1, __nv_bfloat16* dW3, __nv_bfloat16* dW2,
                          int* status, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
-  CUtensorMap mX, mH, mDY, mDG, mDU;
-  if (!map_rows64(&mX, x_perm, H, P) || !map_rows64(&mH, h, F, P) ||
-      !map_rows64(&mDY, dY, H, P) || !map_rows64(&mDG, dg, F, P) || !map_rows64(&mDU, du, F, P))
-    return cudaErrorInvalidValue;
-  // 256 x 256 tiles wherever the sizes allow: measured faster than the
-  // double-buffered 128-wide tiles from 32 to 1024 rows per expert, since the
-  // TMA-store epilogue keeps the unoverlapped part of a tile short.
-  const bool pair = H % 256 == 0 && F % 256 == 0;
-  cudaError_t err = pair ? launch_w<1, true>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s)
-                         : launch_w<1, false>(mH, mDY, mDY, offsets, E, F, H, dW2, dW2, status, s);
+  // Tile shapes.  Wide: 128 rows x 256 columns per launch and B operand (dW1
+  // and dW3 in two launches), two accumulator buffers, so the epilogue of a
+  // tile runs under the MMAs of the next.  Paired: 256 x 256 (dW2) or
+  // 256 x 128 x 2 (dW1, dW3) in one buffer, fewer operand bytes per MMA but the
+  // epilogue only partly hidden.
+  const bool wide = wgrad_wide(P, E);
+  cudaError_t err;
+  if (wide && H % 256 == 0)
+    err = launch_w<1, false, 256>(h, F, dY, dY, H, P, offsets, E, dW2, dW2, status, s);
+  else if (H % 256 == 0 && F % 256 == 0)
+    err = launch_w<1, true, 256>(h, F, dY, dY, H, P, offsets, E, dW2, dW2, status, s);
+  else
+    err = launch_w<1, false, 128>(h, F, dY, dY, H, P, offsets, E, dW2, dW2, status, s);
   if (err != cudaSuccess) return err;
+  if (wide && F % 256 == 0) {
+    err = launch_w<1, false, 256>(x_perm, H, dg, dg, F, P, offsets, E, dW1, dW1, status, s);
+    if (err != cudaSuccess) return err;
+    return launch_w<1, false, 256>(x_perm, H, du, du, F, P, offsets, E, dW3, dW3, status, s);
+  }
   return H % 256 == 0
-             ? launch_w<2, true>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s)
-             : launch_w<2, false>(mX, mDG, mDU, offsets, E, H, F, dW1, dW3, status, s);
+             ? launch_w<2, true, 128>(x_perm, H, dg, du, F, P, offsets, E, dW1, dW3, status, s)
+             : launch_w<2, false, 128>(x_perm, H, dg, du, F, P, offsets, E, dW1, dW3, status, s);
 }
 
 }  // namespace moe

@@ -80,3 +80,39 @@ def test_backward_matches_oracle(name):
     again = moe.moe_backward(dout.cuda(), dev["logits"], dev["W1"], dev["W3"], dev["W2"], k, ws)
     for a, b in zip((dx, dl, dW1, dW3, dW2), again):
         assert torch.equal(a, b)
+
+
+# Rows per expert chosen so that the weight gradients' last K stage ends at
+# every kind of place: inside the first 16-row group, on a 16-row boundary,
+# one past it, at the end of a 64-row stage, one past it; plus an expert with
+# no rows.  Each token goes to one expert (k = 1) through a logit margin.
+TAIL_COUNTS = [1, 15, 16, 17, 31, 48, 63, 64, 65, 127, 128, 129, 0]
+
+
+@pytest.mark.parametrize("H,F", [(256, 512), (384, 384)])
+def test_backward_wgrad_tail_rows(H, F):
+    E, k = len(TAIL_COUNTS), 1
+    labels = np.repeat(np.arange(E), TAIL_COUNTS)
+    rng = np.random.default_rng(5)
+    rng.shuffle(labels)
+    T = labels.size
+    wl = I.small("tail_rows", T=T, H=H, F=F, E=E, k=k)
+    d = I.make_inputs(wl, "cpu")
+    logits = (0.1 * rng.standard_normal((T, E))).astype(np.float32)
+    logits[np.arange(T), labels] += 5.0
+    d["logits"] = torch.from_numpy(logits)
+    assert np.array_equal(np.bincount(O.route_topk(logits, k)[0].reshape(-1), minlength=E),
+                          TAIL_COUNTS)
+    dout = torch.randn(T, H, generator=torch.Generator().manual_seed(32)).to(torch.bfloat16)
+    dev = {n: t.cuda() for n, t in d.items()}
+    ws = moe.Workspace()
+    moe.moe_forward_train(dev["x"], dev["logits"], dev["W1"], dev["W3"], dev["W2"], k, ws)
+    dx, dl, dW1, dW3, dW2 = moe.moe_backward(dout.cuda(), dev["logits"], dev["W1"], dev["W3"],
+                                             dev["W2"], k, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    ref = O.backward(d["x"], logits, d["W1"], d["W3"], d["W2"], k, dout, magnitudes=True)
+    msgs = (mismatches("dx", dx, ref) + mismatches("dlogits", dl, ref) +
+            mismatches("dW1", dW1, ref) + mismatches("dW3", dW3, ref) +
+            mismatches("dW2", dW2, ref))
+    assert not msgs, "\n".join(msgs)
+    assert not dW1[E - 1].any() and not dW3[E - 1].any() and not dW2[E - 1].any()
