@@ -13,43 +13,45 @@ namespace {
 
 constexpr int kDwThreads = 128;
 
-// dY[p] = bf16(w[a] * dout[a / k]), a = sorted_src[p]: one warp per segment of
-// 4 x 32 16-byte vectors of a row, all four loads of a lane in flight before
-// its stores.
+// dY[dest_of[t * k + j]] = bf16(w[t, j] * dout[t]) for every slot j < k:
+// each row of dout is read once (one warp per segment of 4 x 32 16-byte
+// vectors, all four loads of a lane in flight) and stored, scaled, at its k
+// places in expert order.
 constexpr int kScaleUnroll = 4;
 __global__ void __launch_bounds__(256)
-scale_gather_kernel(const __nv_bfloat16* __restrict__ dout, const int32_t* __restrict__ sorted_src,
-                    const float* __restrict__ topk_w, int P, int H, int k,
+scale_gather_kernel(const __nv_bfloat16* __restrict__ dout, const int32_t* __restrict__ dest_of,
+                    const float* __restrict__ topk_w, int T, int H, int k,
                     __nv_bfloat16* __restrict__ dY) {
   const int nv = H / 8;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int upr = (nv + 32 * kScaleUnroll - 1) / (32 * kScaleUnroll);   // segments per row
-  const long long units = (long long)P * upr;
+  const long long units = (long long)T * upr;
   for (long long wu = blockIdx.x * wpb + (threadIdx.x >> 5); wu < units;
        wu += (long long)gridDim.x * wpb) {
-    const int p = (int)(wu / upr);
-    const int v0 = (int)(wu - (long long)p * upr) * 32 * kScaleUnroll + lane;
-    const int a = __ldg(sorted_src + p);
-    const float w = __ldg(topk_w + a);
-    const int4* src = reinterpret_cast<const int4*>(dout + (size_t)(a / k) * H);
-    int4* dst = reinterpret_cast<int4*>(dY + (size_t)p * H);
-    {
-      int4 r[kScaleUnroll];
+    const int t = (int)(wu / upr);
+    const int v0 = (int)(wu - (long long)t * upr) * 32 * kScaleUnroll + lane;
+    const int4* src = reinterpret_cast<const int4*>(dout + (size_t)t * H);
+    float2 f[kScaleUnroll][4];
 #pragma unroll
-      for (int u = 0; u < kScaleUnroll; ++u)
-        if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
+    for (int u = 0; u < kScaleUnroll; ++u) {
+      if (v0 + 32 * u >= nv) continue;
+      const int4 r = __ldg(src + v0 + 32 * u);
+      const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) f[u][c] = __bfloat1622float2(in[c]);
+    }
+    for (int j = 0; j < k; ++j) {
+      const size_t a = (size_t)t * k + j;
+      const float w = __ldg(topk_w + a);
+      int4* dst = reinterpret_cast<int4*>(dY + (size_t)__ldg(dest_of + a) * H);
 #pragma unroll
       for (int u = 0; u < kScaleUnroll; ++u) {
         if (v0 + 32 * u >= nv) continue;
-        const __nv_bfloat162* in = reinterpret_cast<const __nv_bfloat162*>(&r[u]);
         int4 o;
         __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float2 f = __bfloat1622float2(in[c]);
-          po[c] = __floats2bfloat162_rn(w * f.x, w * f.y);
-        }
+        for (int c = 0; c < 4; ++c) po[c] = __floats2bfloat162_rn(w * f[u][c].x, w * f[u][c].y);
         dst[v0 + 32 * u] = o;
       }
     }
@@ -133,14 +135,14 @@ dw_dlogits_kernel(const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* _
 
 }  // namespace
 
-cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* sorted_src,
-                                const float* topk_w, int P, int H, int k, __nv_bfloat16* dY,
+cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* dest_of,
+                                const float* topk_w, int T, int H, int k, __nv_bfloat16* dY,
                                 cudaStream_t s) {
-  if (P == 0) return cudaSuccess;
-  const long long segs = (long long)P * ((H / 8 + 127) / 128);
+  if (T == 0) return cudaSuccess;
+  const long long segs = (long long)T * ((H / 8 + 127) / 128);
   const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
   const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
-  scale_gather_kernel<<<grid, 256, 0, s>>>(dout, sorted_src, topk_w, P, H, k, dY);
+  scale_gather_kernel<<<grid, 256, 0, s>>>(dout, dest_of, topk_w, T, H, k, dY);
   return cudaGetLastError();
 }
 

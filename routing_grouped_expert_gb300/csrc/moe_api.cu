@@ -136,8 +136,8 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   MOE_TRY(mark(2));
   MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s, pdl));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s,
-                        pdl));
+  MOE_TRY(launch_gather_tokens(static_cast<const __nv_bfloat16*>(x), dest_of, T, H, k, x_perm, s,
+                               pdl));
   MOE_TRY(mark(4));
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
@@ -316,6 +316,10 @@ void* mapped_host(const void* p) {
 }
 }  // namespace
 
+#ifndef MOE_HOST_X_IN_PLACE_MAX
+#define MOE_HOST_X_IN_PLACE_MAX (1ull << 62)
+#endif
+
 moe_status moe_forward_host(const void* x_host, const float* logits_host, const void* W1,
                             const void* W3, const void* W2, int T, int H, int F, int E, int k,
                             void* out_host, void* ws, size_t ws_bytes, void* stream) {
@@ -328,13 +332,11 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
   if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // A page-locked, mapped host buffer is used in place: the kernels load the
-  // logits and store the result (each element once) and, for small batches,
-  // load x over the host link, with no staging copy.  The gather reads every
-  // row of x k times, so past kInPlaceBytes of gathered rows one copy into
-  // HBM is cheaper.  Any other host buffer goes through a staging region of ws.
-  constexpr size_t kInPlaceBytes = size_t(32) << 20;
-  const bool small = (size_t)T * k * H * 2 <= kInPlaceBytes;
+  // A page-locked, mapped host buffer is used in place: the kernels load x
+  // and the logits and store the result over the host link, each element
+  // once, with no staging copy (x up to MOE_HOST_X_IN_PLACE_MAX bytes).  Any
+  // other host buffer goes through a staging region of ws.
+  const bool small = (size_t)T * H * 2 <= (size_t)MOE_HOST_X_IN_PLACE_MAX;
   void* xm = small ? mapped_host(x_host) : nullptr;
   void* lm = mapped_host(logits_host);
   void* om = mapped_host(out_host);   // the combine writes each result row once
@@ -468,7 +470,6 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
   const int32_t* topk_idx = ws_ptr<int32_t>(ws, L.topk_idx);
   const float* topk_w = ws_ptr<float>(ws, L.topk_w);
   const int32_t* offsets = ws_ptr<int32_t>(ws, L.offsets);
-  const int32_t* sorted_src = ws_ptr<int32_t>(ws, L.sorted_src);
   const int32_t* dest_of = ws_ptr<int32_t>(ws, L.dest_of);
   const __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
   const __nv_bfloat16* h = ws_ptr<__nv_bfloat16>(ws, L.h);
@@ -481,7 +482,7 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and the split counters of DGrad dx (adjacent) start at zero
   MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
-  MOE_TRY(launch_scale_gather(dout_b, sorted_src, topk_w, P, H, k, dY, s));
+  MOE_TRY(launch_scale_gather(dout_b, dest_of, topk_w, T, H, k, dY, s));
   MOE_TRY(launch_dw_dlogits(dout_b, y, dest_of, topk_idx, router_logits, T, H, E, k, dlogits, s));
   MOE_TRY(launch_dgrad(dY, ws_ptr<__nv_bfloat16>(ws, R.g), ws_ptr<__nv_bfloat16>(ws, R.u),
                        static_cast<const __nv_bfloat16*>(W1),

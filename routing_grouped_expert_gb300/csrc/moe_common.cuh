@@ -246,6 +246,10 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32
 int ffn_block_rows(int P, int E, int H, int F);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s, bool pdl = false);
+// The same rows from the token side: x_perm[dest_of[t * k + j]] = x[t], each
+// row of x read once.
+cudaError_t launch_gather_tokens(const __nv_bfloat16* x, const int32_t* dest_of, int T, int H,
+                                 int k, __nv_bfloat16* x_perm, cudaStream_t s, bool pdl = false);
 // Extra tensors of the grouped-GEMM epilogues that read or write more than
 // their main output.
 struct EpiAux {
@@ -308,8 +312,8 @@ cudaError_t launch_router(const __nv_bfloat16* x, const __nv_bfloat16* Wg, int T
                           cudaStream_t s);
 
 // Backward steps (training).
-cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* sorted_src,
-                                const float* topk_w, int P, int H, int k, __nv_bfloat16* dY,
+cudaError_t launch_scale_gather(const __nv_bfloat16* dout, const int32_t* dest_of,
+                                const float* topk_w, int T, int H, int k, __nv_bfloat16* dY,
                                 cudaStream_t s);
 cudaError_t launch_dw_dlogits(const __nv_bfloat16* dout, const __nv_bfloat16* y,
                               const int32_t* dest_of, const int32_t* topk_idx,

@@ -181,6 +181,38 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ s
   }
 }
 
+// x_perm[dest_of[t * k + j]] = x[t] for every slot j < k: each row of x is
+// read once (one warp per segment of 4 x 32 16-byte vectors, segments
+// grid-strided, all four loads of a lane in flight) and stored at its k
+// places in expert order.
+__global__ void __launch_bounds__(256)
+gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ dest_of,
+                     int T, int H, int k, __nv_bfloat16* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
+  const int nv = H / 8;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int upr = (nv + 32 * kGatherUnroll - 1) / (32 * kGatherUnroll);   // segments per row
+  const long long units = (long long)T * upr;
+  for (long long w = blockIdx.x * wpb + (threadIdx.x >> 5); w < units;
+       w += (long long)gridDim.x * wpb) {
+    const int t = (int)(w / upr);
+    const int v0 = (int)(w - (long long)t * upr) * 32 * kGatherUnroll + lane;
+    const int4* src = reinterpret_cast<const int4*>(x) + (size_t)t * nv;
+    int4 r[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u)
+      if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
+    for (int j = 0; j < k; ++j) {
+      int4* dst = reinterpret_cast<int4*>(x_perm) + (size_t)__ldg(dest_of + (size_t)t * k + j) * nv;
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (v0 + 32 * u < nv) dst[v0 + 32 * u] = r[u];
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
@@ -219,6 +251,16 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int
   const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
   const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
   return launch_k(gather_kernel, dim3(grid), dim3(256), 0, s, pdl, x, sorted_src, P, H, k,
+                  x_perm);
+}
+
+cudaError_t launch_gather_tokens(const __nv_bfloat16* x, const int32_t* dest_of, int T, int H,
+                                 int k, __nv_bfloat16* x_perm, cudaStream_t s, bool pdl) {
+  if (T == 0) return cudaSuccess;
+  const long long segs = (long long)T * ((H / 8 + 127) / 128);
+  const long long want = (segs + 7) / 8;                  // 8 warps (segments) per CTA
+  const int grid = (int)(want < 8LL * device_sm_count() ? want : 8LL * device_sm_count());
+  return launch_k(gather_tokens_kernel, dim3(grid), dim3(256), 0, s, pdl, x, dest_of, T, H, k,
                   x_perm);
 }
 
