@@ -326,7 +326,7 @@ def bench_ours(args, rank, world, local):
     top = max(mean_ms, key=mean_ms.get)
     kbytes = {"route": acc.route_bytes(wl.T, wl.E, wl.k),
               "scan": 0, "scatter": 4 * P * 4,
-              "gather": 2 * P * wl.H * 2,
+              "gather": acc.gather_bytes(wl.T, wl.k, wl.H),
               "fc1": acc.fc1_bytes(wl.H, wl.F, touched, P),
               "fc2": acc.fc2_bytes(wl.H, wl.F, touched, P),
               "combine": acc.combine_bytes(wl.T, wl.H, wl.k)}

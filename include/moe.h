@@ -190,10 +190,9 @@ moe_status moe_forward(const void* x, const float* router_logits,
  * returns the result in out_host [T, H] bf16.  The weights are device
  * pointers (resident model parameters).  A host buffer that is page-locked
  * and mapped into the device's address space (cudaHostAlloc, cudaHostRegister,
- * or a framework's pinned allocation) is used in place: the kernels read the
- * logits, write the result and -- when T*k*H*2 is at most 32 MiB, since the
- * gather reads each row of x k times -- read x across the host-device link,
- * with no staging copy.  Any other host buffer is copied through a staging region of
+ * or a framework's pinned allocation) is used in place: the kernels read x and
+ * the logits and write the result across the host-device link, each element
+ * once, with no staging copy.  Any other host buffer is copied through a staging region of
  * `ws` (moe_workspace_size covers it) with cudaMemcpyAsync.  out_host is
  * valid once `stream` has been synchronised.
  */

@@ -60,9 +60,15 @@ def route_bytes(T: int, E: int, k: int) -> int:
 
 def permute_bytes(T: int, k: int, H: int) -> int:
     """topk_idx read twice (count, scatter) + sorted_src, dest_of written +
-    the x rows gathered into expert order (read and written)."""
+    gather_bytes."""
     P = T * k
-    return 2 * P * INT32 + 2 * P * INT32 + 2 * P * H * BF16
+    return 2 * P * INT32 + 2 * P * INT32 + gather_bytes(T, k, H)
+
+
+def gather_bytes(T: int, k: int, H: int) -> int:
+    """Each row of x read once, written to its k places in expert order (plus
+    dest_of read)."""
+    return T * H * BF16 + T * k * H * BF16 + T * k * INT32
 
 
 def fc1_bytes(H: int, F: int, touched: int, P: int) -> int:
