@@ -218,6 +218,13 @@ struct OutMaps {
   CUtensorMap m[3];
 };
 
+// Token-row tensor maps of the N operand ([P, K], K contiguous), per K phase:
+// boxes of 32, 64, 128 and 256 rows x 64 K, so a block's rows (rounded up to
+// 32) arrive in at most three TMA instructions per stage.
+struct RowMaps {
+  CUtensorMap m[2][4];
+};
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
                                              int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
@@ -244,8 +251,7 @@ template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ RowMaps rows, int a_atoms,
                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ block_off,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
@@ -288,8 +294,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA0);
     if (kGLU || kDualK) prefetch_tmap(&tmA1);
-    prefetch_tmap(&tmB);
-    if (kDualK) prefetch_tmap(&tmB1);
+    for (int ph = 0; ph < (kDualK ? 2 : 1); ++ph)
+      for (int j = 0; j < 4; ++j) prefetch_tmap(&rows.m[ph][j]);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -339,15 +345,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if constexpr (kAKMajor) {
               // 128 weight rows x 64 K, K contiguous: one box
               tma_load_3d(sA + a * kABytes, map, fb, k0, fa, it.e, pol_w);
+            } else if (a_atoms) {
+              // 64 K rows x 128 features, features contiguous, as two 64-feature
+              // atoms of a 4-D view: one box
+              tma_load_4d(sA + a * kABytes, map, fb, 0, k0, fa >> 6, it.e, pol_w);
             } else {
-              // 64 K rows x 64 features per box, features contiguous: two boxes
+              // 64 K rows x 64 features per box: two boxes
               tma_load_3d(sA + a * kABytes, map, fb, fa, k0, it.e, pol_w);
               tma_load_3d(sA + a * kABytes + kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
             }
           }
-          const CUtensorMap* bmap = second ? &tmB1 : &tmB;
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sB + bx * kBBoxBytes, bmap, fb, k0, it.row0 + bx * kRowBox, pol_x);
+          // the block's rows, rounded up to 32, in boxes of 256, 128, 64 and 32 rows
+          const CUtensorMap* bm = rows.m[second ? 1 : 0];
+          for (int r = 0; r < nbox * kRowBox;) {
+            const int rem = nbox * kRowBox - r;
+            const int lg = (kBN >= 256 && rem >= 256) ? 3 : (kBN >= 128 && rem >= 128) ? 2
+                                                                : rem >= 64             ? 1
+                                                                                        : 0;
+            tma_load_2d(sB + r * 128, &bm[lg], fb, k0, it.row0 + r, pol_x);
+            r += kRowBox << lg;
+          }
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -730,7 +747,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -757,9 +774,20 @@ bool make_tensor_map_bf16(void* map, const void* base, int rank, const unsigned 
 
 namespace {
 
+// A weight operand's tensor map; `atoms`: a 4-D view (64 features, K rows,
+// 64-feature atoms, experts) whose one box covers a 128-feature tile.
+struct WMap {
+  CUtensorMap m;
+  bool atoms;
+};
+// A token-row operand's tensor maps (boxes of 32, 64, 128, 256 rows).
+struct RowMap4 {
+  CUtensorMap h[4];
+};
+
 template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false, bool kDualK = false>
-cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const CUtensorMap& b1, const int32_t* offsets, const int32_t* block_off,
+cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const RowMap4& b1,
+                        const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
                         const OutMaps& outs, int* status, cudaStream_t s,
@@ -776,9 +804,14 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   const int grid = (int)(items < device_sm_count() ? items : device_sm_count());
   if (grid > kStreamKMaxCtas || (size_t)kNumA * BM * kBN * 4 > sk.slot_bytes)
     sk = StreamK{nullptr, nullptr, 0};
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0, a1, b, b1, offsets, block_off, num_blocks,
-                                             block_expert, n_mt, K, out, ld_out, M_total, aux,
-                                             outs, sk, status);
+  RowMaps rm;
+  for (int j = 0; j < 4; ++j) {
+    rm.m[0][j] = b.h[j];
+    rm.m[1][j] = b1.h[j];
+  }
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0.m, a1.m, rm, a0.atoms ? 1 : 0, offsets, block_off,
+                                             num_blocks, block_expert, n_mt, K, out, ld_out,
+                                             M_total, aux, outs, sk, status);
   return cudaGetLastError();
 }
 
@@ -796,32 +829,47 @@ struct PlanPtrs {
   const int32_t* block_expert;
 };
 
-// Weights as the MN-major M operand ([E, K, M] memory, M contiguous): boxes of
-// 64 features x 64 K rows.
-bool map_weights_mn(CUtensorMap* m, const void* W, int K, int M, int E) {
+// Weights as the MN-major M operand ([E, K, M] memory, M contiguous).  With M
+// a multiple of 64: a 4-D view (64 features, K rows, M / 64 atoms, E) and
+// boxes of two atoms x 64 K rows, one per 128-feature tile; otherwise (the
+// router's narrow W_g) boxes of 64 features x 64 K rows, the features past M
+// zero-filled.
+bool map_weights_mn(WMap* m, const void* W, int K, int M, int E) {
+  m->atoms = M % 64 == 0;
+  if (m->atoms) {
+    const cuuint64_t d[4] = {64, (cuuint64_t)K, (cuuint64_t)M / 64, (cuuint64_t)E};
+    const cuuint64_t st[3] = {(cuuint64_t)M * 2, 128, (cuuint64_t)K * M * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)BK, 2, 1};
+    return make_map(&m->m, W, 4, d, st, box);
+  }
   const cuuint64_t d[3] = {(cuuint64_t)M, (cuuint64_t)K, (cuuint64_t)E};
   const cuuint64_t st[2] = {(cuuint64_t)M * 2, (cuuint64_t)K * M * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)BK, 1};
-  return make_map(m, W, 3, d, st, box);
+  return make_map(&m->m, W, 3, d, st, box);
 }
 // Weights as the K-major M operand ([E, M, K] memory, K contiguous): boxes of
 // 128 rows x 64 K.
-bool map_weights_k(CUtensorMap* m, const void* W, int M, int K, int E) {
+bool map_weights_k(WMap* m, const void* W, int M, int K, int E) {
+  m->atoms = false;
   const cuuint64_t d[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)E};
   const cuuint64_t st[2] = {(cuuint64_t)K * 2, (cuuint64_t)M * K * 2};
   const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1};
-  return make_map(m, W, 3, d, st, box);
+  return make_map(&m->m, W, 3, d, st, box);
 }
-// Token rows [P, K] (K contiguous) as the N operand: boxes of 32 rows x 64 K.
-bool map_rows(CUtensorMap* m, const void* X, int K, int P) {
+// Token rows [P, K] (K contiguous) as the N operand: boxes of 32, 64, 128 and
+// 256 rows x 64 K.
+bool map_rows(RowMap4* m, const void* X, int K, int P) {
   const cuuint64_t d[2] = {(cuuint64_t)K, (cuuint64_t)P};
   const cuuint64_t st[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)kRowBox};
-  return make_map(m, X, 2, d, st, box);
+  for (int j = 0; j < 4; ++j) {
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)(kRowBox << j)};
+    if (!make_map(&m->h[j], X, 2, d, st, box)) return false;
+  }
+  return true;
 }
 
 template <int kBN, int kBufs1>
-cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUtensorMap& mX,
+cudaError_t launch_fc1(const WMap& mW1, const WMap& mW3, const RowMap4& mX,
                        const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
                        const EpiAux* save, int* status, cudaStream_t s, StreamK sk) {
   const long long nb_max = max_blocks(P, E, kBN);
@@ -840,7 +888,7 @@ cudaError_t launch_fc1(const CUtensorMap& mW1, const CUtensorMap& mW3, const CUt
 }
 
 template <int kNumA, int kBN, int kBufs>
-cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const PlanPtrs& pl, int P,
+cudaError_t launch_fc2(const WMap& mW2, const RowMap4& mH, const PlanPtrs& pl, int P,
                        int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s,
                        StreamK sk = StreamK{nullptr, nullptr, 0}) {
   OutMaps om;
@@ -855,9 +903,9 @@ cudaError_t launch_fc2(const CUtensorMap& mW2, const CUtensorMap& mH, const Plan
 // in the dh / dx products; worth it for large blocks, whose long K keeps the
 // unoverlapped epilogue a small share of a tile.
 template <int kBN, bool kPairF, bool kPairH>
-cudaError_t launch_dgrad_t(const CUtensorMap& mW2k, const CUtensorMap& mDY,
-                           const CUtensorMap& mW1k, const CUtensorMap& mW3k,
-                           const CUtensorMap& mDG, const CUtensorMap& mDU, const PlanPtrs& pl,
+cudaError_t launch_dgrad_t(const WMap& mW2k, const RowMap4& mDY, const WMap& mW1k,
+                           const WMap& mW3k, const RowMap4& mDG, const RowMap4& mDU,
+                           const PlanPtrs& pl,
                            int P, int H, int F, int E, const EpiAux& aux,
                            __nv_bfloat16* dx_perm, int* status, cudaStream_t s,
                            StreamK sk = StreamK{nullptr, nullptr, 0}) {
@@ -899,7 +947,8 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save,
                                const StreamKSpace* sks) {
   if (P == 0) return cudaSuccess;
-  CUtensorMap mW1, mW3, mW2, mX, mH;
+  WMap mW1, mW3, mW2;
+  RowMap4 mX, mH;
   if (!map_weights_mn(&mW1, W1, H, F, E) || !map_weights_mn(&mW3, W3, H, F, E) ||
       !map_weights_mn(&mW2, W2, F, H, E) || !map_rows(&mX, x_perm, H, P) ||
       !map_rows(&mH, h, F, P))
@@ -937,7 +986,8 @@ cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const 
   if (P == 0) return cudaSuccess;
   const StreamK sk =
       sks ? StreamK{sks->part, sks->cnt, sks->slot_bytes} : StreamK{nullptr, nullptr, 0};
-  CUtensorMap mW2k, mW1k, mW3k, mDY, mDG, mDU;
+  WMap mW2k, mW1k, mW3k;
+  RowMap4 mDY, mDG, mDU;
   if (!map_weights_k(&mW2k, W2, F, H, E) || !map_weights_k(&mW1k, W1, H, F, E) ||
       !map_weights_k(&mW3k, W3, H, F, E) || !map_rows(&mDY, dY, H, P) ||
       !map_rows(&mDG, dg, F, P) || !map_rows(&mDU, du, F, P))
@@ -974,7 +1024,8 @@ cudaError_t launch_router_gemm(const __nv_bfloat16* x, const __nv_bfloat16* Wg, 
                                float* logits, int* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   // logits^T = Wg^T x^T: one "expert" whose weight matrix is Wg [H, E]
-  CUtensorMap mG, mX;
+  WMap mG;
+  RowMap4 mX;
   if (!map_weights_mn(&mG, Wg, H, E, 1) || !map_rows(&mX, x, H, T)) return cudaErrorInvalidValue;
   const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
   switch (ffn_mode(T, 1)) {
