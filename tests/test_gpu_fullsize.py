@@ -47,11 +47,11 @@ def test_full_size_workload(name):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("name", ["mixtral_decode", "dbrx_prefill"])
+@pytest.mark.parametrize("name", ["mixtral_decode", "dbrx_prefill", "fine_grained"])
 def test_full_size_host_buffers(name):
-    """moe_forward_host with pinned host buffers gives moe_forward's bits: the
-    decode batch reads x in place, the prefill chunk (past the in-place size)
-    stages x through the workspace; both write the result in place."""
+    """moe_forward_host with pinned host buffers gives moe_forward's bits: x and
+    the logits are read and the result written in place across the host link
+    (117 MB of x at the fine-grained size, each row read once by the gather)."""
     wl = I.WORKLOADS[name]
     d = I.make_inputs(wl, "cuda")
     out = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k)
