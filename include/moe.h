@@ -24,8 +24,9 @@
  *   - `ws` is a caller-owned device workspace of at least
  *     moe_workspace_size(T, H, F, E, k) bytes, 256-byte aligned.  It holds
  *     the intermediates (gathered rows, expert activations and outputs),
- *     8 to 32 MiB of partial tiles for the balanced K split of FC2, and a
- *     device status word.  Its contents need no initialisation.  Calls that
+ *     8 to 32 MiB of partial tiles for the balanced K split of FC2, the
+ *     head of the grouped GEMM's tile queue, and a device status word.  Its
+ *     contents need no initialisation (each layer call clears the counters).  Calls that
  *     share one workspace must not overlap in time (use one stream per
  *     workspace).
  *   - Limits: 0 <= T, T*k < 2^31; 1 <= E <= MOE_MAX_EXPERTS;

@@ -233,7 +233,7 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and FC2's split counters (adjacent) start at zero
-  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
+  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kSkCntInts * sizeof(int), s));
   MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert,
                       ffn_block_rows(P, E, H, F), s));
   MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
@@ -481,7 +481,7 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
   const auto* dout_b = static_cast<const __nv_bfloat16*>(dout);
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and the split counters of DGrad dx (adjacent) start at zero
-  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kStreamKMaxCtas * sizeof(int), s));
+  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kSkCntInts * sizeof(int), s));
   MOE_TRY(launch_scale_gather(dout_b, dest_of, topk_w, T, H, k, dY, s));
   MOE_TRY(launch_dw_dlogits(dout_b, y, dest_of, topk_idx, router_logits, T, H, E, k, dlogits, s));
   MOE_TRY(launch_dgrad(dY, ws_ptr<__nv_bfloat16>(ws, R.g), ws_ptr<__nv_bfloat16>(ws, R.u),

@@ -78,10 +78,13 @@ __device__ __forceinline__ void set_status(int* status, int code, int detail = 0
 // CTAs whose FC2 partial tiles the workspace has room for (a launch with a
 // larger grid does not split tiles).
 constexpr int kStreamKMaxCtas = 256;
+// The split counters are followed by the grouped GEMM's tile-queue head (one
+// int, padded to 128 bytes); all are zero between launches.
+constexpr int kSkCntInts = kStreamKMaxCtas + 32;
 
 struct WsLayout {
   size_t status;        // int32[64]
-  size_t sk_cnt;        // int32[kStreamKMaxCtas]   FC2 split counters (cleared with status)
+  size_t sk_cnt;        // int32[kSkCntInts]   split counters, then the tile-queue head (cleared with status)
   size_t topk_idx;      // int32[P]
   size_t topk_w;        // f32[P]
   size_t counts;        // int32[E]
@@ -138,7 +141,7 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
   L.status = take(64 * 4);
-  L.sk_cnt = take((size_t)kStreamKMaxCtas * 4);
+  L.sk_cnt = take((size_t)kSkCntInts * 4);
   L.chunk_base = take(C * E * 4);   // after status and sk_cnt: one memset clears all three
   L.topk_idx = take(P * 4);
   L.topk_w = take(P * 4);
@@ -259,11 +262,12 @@ struct EpiAux {
   __nv_bfloat16* du;
   int ld;
 };
-// Scratch of FC2's balanced K split: partial tiles and boundary counters.  The
-// counters must be zero before a launch; every launch leaves them zero.
+// Scratch of the grouped GEMM: partial tiles and boundary counters of the
+// balanced K split, and the head of the tile queue.  The counters must be zero
+// before a launch; every launch that completes leaves them zero.
 struct StreamKSpace {
   float* part;         // [kStreamKMaxCtas][2] slots of slot_bytes (fp32 partial tiles)
-  int* cnt;            // [kStreamKMaxCtas]
+  int* cnt;            // [kSkCntInts]: split counters, then the queue head at kStreamKMaxCtas
   size_t slot_bytes;
 };
 // FC1 (+SwiGLU) and FC2 over the expert groups.  With `save`, FC1 also keeps
