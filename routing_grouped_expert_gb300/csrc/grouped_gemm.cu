@@ -17,12 +17,14 @@
 // operand (N = rows rounded up to 16), so a skinny decode block costs no
 // padded MMA work.
 //
-// Scheduling: every CTA is persistent (one per SM) and walks the flat tile
-// list round-robin.  Tiles are ordered expert-major, then in groups of up to
-// 16 blocks of that expert, then feature tile, then block: the blocks of a
-// hot expert are spread over all SMs and run side by side on the same weight
-// tile, the single-GPU counterpart of replicating a hot expert
-// ("MegaScale-Infer", §3.4 Load Balancing; "MegaFlux", §3.1-3.2).
+// Scheduling: every CTA is persistent (one per SM) and takes tiles of the
+// flat tile list from an on-device queue (a counter advanced once per tile)
+// or, where that measured slower, round-robin.  Tiles are ordered
+// expert-major, then in groups of up to 16 blocks of that expert, then
+// feature tile, then block: the blocks of a hot expert are spread over all
+// SMs and run side by side on the same weight tile, the single-GPU
+// counterpart of replicating a hot expert ("MegaScale-Infer", §3.4 Load
+// Balancing; "MegaFlux", §3.1-3.2).
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2-9 = epilogue (TMEM -> registers -> global): two warps

@@ -5,27 +5,28 @@
 // i.e. D[m, n] = sum over the expert's rows p of A[p, m] * B[p, n].
 //
 // Tile = (expert, rows m of dW, columns n of dW); K = the expert's rows in
-// stages of 64.  Two tile shapes: with kPairM (used whenever the sizes are
-// multiples of 256), 256 x 256 (two 128-row A sub-tiles sharing the B
-// columns) in one TMEM buffer, which halves the operand bytes staged per MMA
-// and so keeps the tensor core fed; otherwise 128 x 128 per B operand with
-// two accumulator buffers (the epilogue of one tile overlaps the MMAs of the
-// next).  Both operands
-// are row-major [P, *] buffers read as MN-major tensor-core operands by TMA
-// boxes of 64 rows x 64 columns.  The
-// last stage of an expert usually runs past its rows into the next expert's:
-// its MMAs stop at the last 16-row K group holding rows of the expert, and
-// the MMA warp zeroes the rest of that group in shared memory (whole 128-byte
-// rows, so the swizzle does not matter), then fences it for the tensor core.
+// stages of 64.  Tile shapes: with few rows per expert, 128 rows x 256
+// columns per B operand with two accumulator buffers (the epilogue of one tile
+// overlaps the MMAs of the next; dW1 and dW3 in two launches); otherwise,
+// with kPairM (whenever the sizes are multiples of 256), 256 x 256 (two
+// 128-row A sub-tiles sharing the B columns) in one TMEM buffer, which halves
+// the operand bytes staged per MMA; else 128 x 128 per B operand with two
+// buffers.  Both operands are row-major [P, *] buffers read as MN-major
+// tensor-core operands, one TMA box per operand and stage (a 3-D view: 64
+// columns, rows, 64-column atoms).  The last stage of an expert usually runs
+// past its rows into the next expert's: its MMAs stop at the last 16-row K
+// group holding rows of the expert, and a warp of its own zeroes the rest of
+// that group in shared memory (whole 128-byte rows, so the swizzle does not
+// matter) and fences it for the tensor core before handing the stage on.
 // Experts without rows get zero gradients.
 //
-// Warp roles as in the forward engine: warp 0 TMA producer, warp 1 MMA
-// (all lanes help zero the tail; lane 0 issues), warps 2-9 epilogue.  The
-// epilogue converts 32 rows x 64 columns at a time to bf16 in a 128-byte-
-// swizzled staging buffer of its own (4 KB per warp) and writes it with a
-// TMA store, so the gradient leaves in whole lines without holding the warp;
-// the accumulator buffer is released as soon as its last columns are read.
-// Every wait is bounded and reports MOE_ERR_TIMEOUT.
+// Warp roles: warp 0 TMA producer, warp 1 MMA (lane 0 issues), warps 2-9
+// epilogue, warp 10 tail rows.  The epilogue converts 32 rows x 64 columns
+// at a time to bf16 in a 128-byte-swizzled staging buffer of its own (4 KB
+// per warp) and writes it with a TMA store, so the gradient leaves in whole
+// lines without holding the warp; each 128-column group of the accumulator is
+// handed back as soon as it is read, the next chunk read before the current
+// one is stored.  Every wait is bounded and reports MOE_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "moe_common.cuh"
