@@ -309,9 +309,10 @@ def bench_ours(args, rank, world, local):
                "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                "d2h_bytes_per_step": wl.T * wl.H * 2,
                "ms_per_step": e2e_ms / K,
-               "note": "moe_forward_host: pinned host x and logits copied in, result copied "
-                       "out, inside the timed region" + (", L2 flushed between steps" if flush
-                                                         else "")}
+               "note": "moe_forward_host on pinned host buffers: x and the logits are read and "
+                       "the result written across the host link by the kernels (each byte "
+                       "once), inside the timed region" + (", L2 flushed between steps"
+                                                           if flush else "")}
 
     if rank != 0:
         return None
