@@ -102,14 +102,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Prefetch one box of a 3-D tensor into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // L2 eviction-priority policies for the cache hints.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
