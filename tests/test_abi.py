@@ -77,3 +77,62 @@ def test_host_validation_rejects_before_any_launch():
     # empty batch is a no-op that touches nothing
     assert lib.moe_forward(None, None, p, p, p, 0, 512, 1024, 8, 2, None, None, 0, None) == 0
     assert lib.moe_combine(None, None, None, 0, 512, 2, None, None) == 0
+
+
+def test_host_validation_of_the_other_entry_points():
+    """Every entry point checks sizes, pointers and the workspace on the host,
+    in that order, before anything is enqueued (nothing here needs a GPU)."""
+    lib = binding.load_library()
+    p = ctypes.c_void_p(4096)          # never dereferenced: rejected first
+    big = 1 << 40
+    INVALID, WS, OK = 1, 4, 0
+    # permute: sizes, then the outputs (counts/offsets even for T = 0), then ws
+    assert lib.moe_permute(p, 16, 8, 9, p, p, p, p, p, big, None) == INVALID      # k > E
+    assert lib.moe_permute(p, 16, 8, 2, None, p, p, p, p, big, None) == INVALID   # counts
+    assert lib.moe_permute(None, 16, 8, 2, p, p, p, p, p, big, None) == INVALID   # topk_idx
+    assert lib.moe_permute(p, 16, 8, 2, p, p, p, p, p, 64, None) == WS
+    assert lib.moe_permute(None, 0, 8, 2, p, p, None, None, None, 0, None) == WS  # T=0 needs ws
+    # grouped FFN
+    assert lib.moe_grouped_ffn(p, p, p, p, p, p, 16, 500, 1024, 8, 2, p, p, big, None) == INVALID
+    assert lib.moe_grouped_ffn(p, p, p, p, p, p, 16, 512, 1024, 8, 2, None, p, big, None) == INVALID
+    assert lib.moe_grouped_ffn(p, p, p, p, p, p, 16, 512, 1024, 8, 2, p, p, 64, None) == WS
+    assert lib.moe_grouped_ffn(None, None, None, p, p, p, 0, 512, 1024, 8, 2, None, None, 0,
+                               None) == OK
+    # host-buffer forward
+    assert lib.moe_forward_host(p, p, p, p, p, 16, 512, 1000, 8, 2, p, p, big, None) == INVALID
+    assert lib.moe_forward_host(None, p, p, p, p, 16, 512, 1024, 8, 2, p, p, big, None) == INVALID
+    assert lib.moe_forward_host(p, p, p, p, p, 16, 512, 1024, 8, 2, p, p, 64, None) == WS
+    assert lib.moe_forward_host(None, None, p, p, p, 0, 512, 1024, 8, 2, None, None, 0,
+                                None) == OK
+    # router projection: H a multiple of 128, E within range (a multiple of 8 from 64 on)
+    assert lib.moe_router_logits(p, p, 16, 500, 8, p, p, big, None) == INVALID
+    assert lib.moe_router_logits(p, p, 16, 512, 100, p, p, big, None) == INVALID
+    assert lib.moe_router_logits(p, None, 16, 512, 8, p, p, big, None) == INVALID
+    assert lib.moe_router_logits(p, p, 16, 512, 8, p, p, 16, None) == WS
+    assert lib.moe_router_logits(None, None, 0, 512, 8, None, None, 0, None) == OK
+    # gated layer: the shared expert's three matrices come together or not at all
+    wsg = binding.moe_workspace_size_gated
+    assert wsg(16, 512, 1024, 256, 8, 2) > binding.moe_workspace_size(16, 512, 1024, 8, 2)
+    assert wsg(16, 512, 1024, 200, 8, 2) == 0          # Fs not a multiple of 128
+    assert wsg(16, 512, 1024, 0, 100, 2) == 0          # E >= 64 not a multiple of 8
+    assert lib.moe_forward_gated(p, p, p, p, p, p, None, p, 16, 512, 1024, 256, 8, 2, p, p, big,
+                                 None) == INVALID
+    assert lib.moe_forward_gated(p, p, p, p, p, None, None, None, 16, 512, 1024, 0, 8, 2, p, p,
+                                 64, None) == WS
+    # training forward and backward
+    wst = binding.moe_workspace_size_train
+    assert wst(16, 512, 1024, 8, 2) > binding.moe_workspace_size(16, 512, 1024, 8, 2)
+    assert wst(16, 512, 1024, 8, 9) == 0
+    assert lib.moe_forward_train(p, p, p, p, p, 16, 512, 1024, 8, 2, p, p, 64, None) == WS
+    assert lib.moe_forward_train(p, None, p, p, p, 16, 512, 1024, 8, 2, p, p, big,
+                                 None) == INVALID
+    assert lib.moe_backward(p, p, p, p, p, 16, 512, 1024, 8, 2, p, None, p, p, p, p, big,
+                            None) == INVALID           # dlogits
+    assert lib.moe_backward(p, p, p, p, p, 16, 512, 1024, 8, 2, p, p, p, p, p, p, 64,
+                            None) == WS
+    assert lib.moe_backward(None, None, p, p, p, 0, 512, 1024, 8, 2, None, None, None, None,
+                            None, None, 0, None) == OK
+    # stage names of the per-stage forward
+    n = [lib.moe_forward_stage_name(i) for i in range(-1, 9)]
+    assert n[0] is None and n[1] == b"route" and b"fc1" in n and b"combine" in n
+    assert n[-1] is None
