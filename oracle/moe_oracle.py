@@ -295,10 +295,17 @@ def backward(x, logits, W1, W3, W2, k: int, dout, magnitudes: bool = False):
 
     With magnitudes=True it also returns, under "mag_<name>", the first-order
     size, in units of eps, of the change that rounding the stored operands
-    (dY, g, u, h, dg, du) by a relative eps makes to each gradient: sums over
-    absolute values that follow each rounding through the chain rule, e.g.
-    for dW1 the rounding of dY through dh, of u, of g through the SwiGLU
-    derivative (whose factor crosses zero near g = -1.28), and of dg."""
+    (dY, g, u, h, y, dg, du and the per-assignment dx rows) by a relative eps
+    makes to each gradient: sums over absolute values that follow each
+    rounding through the chain rule, e.g. for dW1 the rounding of dY through
+    dh, of u, of g through the SwiGLU derivative (whose factor crosses zero
+    near g = -1.28), and of dg; for dW2 the rounding of h and of dY; for dx
+    also the rounding of each assignment's row before the sum over slots; for
+    the routing-weight gradient the rounding of h through y and of y.  For
+    dW1, dW3, dW2 and dlogits this is the largest first-order change over all
+    signs of the roundings; for dx it is an upper bound of it (the rounding of
+    dY is followed through dh with the triangle inequality taken inside the
+    sum over features)."""
     l = np.asarray(logits, dtype=np.float32)
     T, E = l.shape
     idx, w = route_topk(l, k)
@@ -349,9 +356,13 @@ def backward(x, logits, W1, W3, W2, k: int, dout, magnitudes: bool = False):
             m_du = m_dh * np.abs(g * s) + np.abs(dh * g * gsp) + np.abs(du)
             mag["dW1"].append(_mm(aX.T, m_dg))
             mag["dW3"].append(_mm(aX.T, m_du))
-            mag["dW2"].append(_mm(ah.T, adY))
-            np.add.at(mdx, t, _mm(m_dg, np.abs(W1e).T) + _mm(m_du, np.abs(W3e).T))
-            mdw[t, j] = np.sum(np.abs(d64[t]) * _mm(ah, np.abs(W2e)), axis=1)
+            mag["dW2"].append(2.0 * _mm(ah.T, adY))             # h and dY rounded
+            dxp = _mm(dg, W1e.T) + _mm(du, W3e.T)               # this expert's dx rows
+            np.add.at(mdx, t, _mm(m_dg, np.abs(W1e).T) + _mm(m_du, np.abs(W3e).T)
+                      + np.abs(dxp))
+            # dw = <dout, y>: h rounded (through y = h W2) and y rounded
+            mdw[t, j] = (np.sum(ah * np.abs(_mm(d64[t], W2e.T)), axis=1)
+                         + np.sum(np.abs(d64[t] * Y), axis=1))
     # exact softmax of the selected logits for the Jacobian
     sel = np.take_along_axis(l.astype(np.float64), idx.astype(np.int64), axis=1)
     ex = np.exp(sel - sel[:, :1])
@@ -362,7 +373,10 @@ def backward(x, logits, W1, W3, W2, k: int, dout, magnitudes: bool = False):
     r = dict(dx=dx, dlogits=dlogits, dw=dw, dW1=np.stack(grads["dW1"]),
              dW3=np.stack(grads["dW3"]), dW2=np.stack(grads["dW2"]))
     if magnitudes:
-        msel = p_exact * (mdw + np.sum(p_exact * mdw, axis=1, keepdims=True))
+        # dl_j = p_j ((1 - p_j) dw_j - sum_{i != j} p_i dw_i); each slot's dw
+        # depends on roundings of its own rows only
+        msel = p_exact * ((1.0 - 2.0 * p_exact) * mdw
+                          + np.sum(p_exact * mdw, axis=1, keepdims=True))
         mdl = np.zeros((T, E))
         np.put_along_axis(mdl, idx.astype(np.int64), msel, axis=1)
         r.update(mag_dx=mdx, mag_dlogits=mdl, mag_dW1=np.stack(mag["dW1"]),
