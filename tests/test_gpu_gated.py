@@ -1,8 +1,12 @@
 """The steps either side of the routed path on the GPU: the router projection
 logits = x @ Wg and the layer from hidden states with an optional shared
-expert, against the oracle.  Routing is an integer decision taken on fp32
-logits, so the oracle ranks on the GPU's own router output; the logits
-themselves are compared with the oracle's fp64 product."""
+expert, against the oracle.  The logits are compared with the oracle's fp64
+product.  Routing is an integer decision taken on fp32 logits: the GPU's
+top-k on its own logits must equal the oracle's top-k on the oracle's logits
+(rounded to fp32) for every token whose decision is not within the logit
+tolerance of a tie; the few that are are counted and reported.  The layer's
+output is then compared with the oracle ranked on the GPU's router output, so
+that such near-ties do not make the comparison of the FFN arithmetic moot."""
 import math
 
 import numpy as np
@@ -31,6 +35,36 @@ CASES = {  # name: (T, H, F, E, k, Fs)
 }
 
 
+def near_tie_tokens(ref_logits32, k, err):
+    """Tokens whose top-k decision (the set and the slot order) could differ
+    between the oracle's fp32 logits and logits within `err` of the exact
+    product: two neighbours in the descending order of the first k+1 logits
+    closer than 2 (err + one fp32 rounding)."""
+    l = np.sort(np.asarray(ref_logits32, np.float64), axis=1)[:, ::-1]
+    top = l[:, :min(k + 1, l.shape[1])]
+    gaps = top[:, :-1] - top[:, 1:]
+    band = 2 * (err + 2.0 ** -24 * np.abs(top[:, :-1]))
+    return np.nonzero((gaps <= band).any(axis=1))[0] if gaps.size else np.zeros(0, int)
+
+
+def check_routing_against_oracle(name, gpu_logits, ref_logits, k):
+    """GPU top-k on the GPU's logits vs oracle top-k on the oracle's fp32
+    logits: equal on every token that is not near a tie, given the largest
+    logit error seen."""
+    ref32 = np.asarray(ref_logits, np.float32)
+    err = float(np.abs(gpu_logits.double().cpu().numpy() - ref_logits).max())
+    got = moe.moe_route_topk(gpu_logits, k)[0].cpu().numpy()
+    want = O.route_topk(ref32, k)[0]
+    near = set(near_tie_tokens(ref32, k, err).tolist())
+    diff = np.nonzero((got != want).any(axis=1))[0]
+    unexplained = [int(t) for t in diff if t not in near]
+    assert not unexplained, (f"{name}: routing differs from the oracle's on tokens "
+                             f"{unexplained[:8]} that are not near a tie")
+    print(f"{name}: max logit error {err:.2e}; {len(near)} of {len(got)} tokens near a tie, "
+          f"{len(diff)} routed differently")
+    assert len(near) <= 2 + len(got) // 100, (name, len(near))
+
+
 def make(name):
     T, H, F, E, k, Fs = CASES[name]
     wl = I.small(name, T=T, H=H, F=F, E=E, k=k)
@@ -53,6 +87,7 @@ def test_gated_layer_matches_oracle(name):
     ref_l = O.router_logits(d["x"], d["Wg"])
     err = np.abs(logits.double().cpu().numpy() - ref_l)
     assert np.all(err <= LOGIT_ATOL + LOGIT_RTOL * np.abs(ref_l)), err.max()
+    check_routing_against_oracle(name, logits, ref_l, wl.k)
     ws = moe.Workspace()
     out = moe.moe_forward_gated(dev["x"], dev["Wg"], dev["W1"], dev["W3"], dev["W2"], wl.k,
                                 shared=shared, ws=ws)
@@ -97,6 +132,7 @@ def test_gated_layer_full_size(name):
     ref_l = O.router_logits(d["x"].cpu(), Wg.cpu())
     err = np.abs(logits.double().cpu().numpy() - ref_l)
     assert np.all(err <= LOGIT_ATOL + LOGIT_RTOL * np.abs(ref_l)), err.max()
+    check_routing_against_oracle(name, logits, ref_l, wl.k)
     rng = np.random.default_rng(2)
     tok = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, 4, replace=False)]))
     ref = O.forward_direct(d["x"], logits.cpu().numpy(), d["W1"], d["W3"], d["W2"], wl.k,
