@@ -6,10 +6,15 @@ SwiGLU FFN -> combine) through libmoe's C ABI.
                     [--impl ours|reference]
 
 One step = one whole-layer forward over the workload's batch of T tokens
-(all four steps of the layer).  Prints ONE JSON line (rank 0).  Under
-torchrun every rank runs the same workload on its own GPU with no data-path
-collective (independent replicas, weak scaling); `value` is the tokens of
-all ranks divided by the slowest rank's time.
+(all four steps of the layer).  The default workload is the largest
+single-GPU one, `fine_grained` (T=8192, H=7168, F=2048, E=256, k=8).  Prints
+ONE JSON line (rank 0): the value and the kernel breakdown of that workload,
+`configs` with every other workload of record measured in the same process,
+and `protocol` with the median and spread of the time per step over three
+input realizations in this process and in a fresh one.  Under torchrun every
+rank runs the same workload on its own GPU with no data-path collective
+(independent replicas, weak scaling); `value` is the tokens of all ranks
+divided by the slowest rank's time.
 
 `--impl reference` times the CPU oracle (fp64, the machine's host cores) on a
 bounded sample of the same workload.
@@ -45,10 +50,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mixtral_decode", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default="fine_grained", choices=sorted(I.WORKLOADS))
     ap.add_argument("--shape", default=None,
                     help="T,H,F,E,k: a uniform-routing workload of these sizes instead")
     ap.add_argument("--sweep", action="store_true",
@@ -58,10 +63,18 @@ def parse():
     ap.add_argument("--gated", action="store_true",
                     help="time the layer from hidden states (router projection + routed "
                          "experts + --shared-f shared expert) instead (own JSON line)")
+    ap.add_argument("--shard-f", action="store_true",
+                    help="time the layer split over the ranks along the FFN features: each "
+                         "rank's fp32 partial, one all-reduce, one rounding (own JSON line)")
     ap.add_argument("--shared-f", type=int, default=0,
                     help="FFN width of the shared expert for --gated (0 = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads of record (the `configs` key)")
+    ap.add_argument("--no-protocol", action="store_true",
+                    help="skip the median over realizations and processes (`protocol` key)")
+    ap.add_argument("--protocol-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.shape:
         T, H, F, E, k = (int(v) for v in args.shape.split(","))
@@ -204,49 +217,61 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ our kernels
-def bench_ours(args, rank, world, local):
-    import routing_grouped_expert_gb300 as moe
-    import torch.distributed as dist
+OTHER_CONFIGS = ("tiny", "mixtral_decode", "dbrx_prefill", "fine_grained", "skewed",
+                 "skewed_10x")
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    wl = I.WORKLOADS[args.workload]
-    d = I.make_inputs(wl, dev)
-    x, logits, W1, W3, W2 = d["x"], d["logits"], d["W1"], d["W3"], d["W2"]
-    ws = moe.Workspace(dev)
-    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
-    P = wl.T * wl.k
 
-    # routing statistics for the byte accounting (not timed)
-    idx, _ = moe.moe_route_topk(logits, wl.k, ws=ws)
+class Inputs:
+    """Inputs of the workloads measured in one run.  Workloads of the same
+    shape and realization share one copy of the weights (the seeds depend on
+    nothing else), so the skewed workloads reuse the fine-grained weights."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.weights = {}
+
+    def get(self, wl):
+        key = (wl.H, wl.F, wl.E, wl.realization)
+        if key not in self.weights:
+            self.weights = {k: v for k, v in self.weights.items() if k[3] == 0}
+            torch.cuda.empty_cache()
+            self.weights[key] = I.make_weights(wl, self.dev)
+        W1, W3, W2 = self.weights[key]
+        return dict(x=I.make_x(wl, self.dev), logits=I.make_logits(wl).to(self.dev),
+                    W1=W1, W3=W3, W2=W2)
+
+
+def routing_stats(moe, wl, d, ws):
+    idx, _ = moe.moe_route_topk(d["logits"], wl.k, ws=ws)
     counts = moe.moe_permute(idx, wl.E, ws=ws)[0].cpu()
-    touched = int((counts > 0).sum())
-    max_count = int(counts.max())
+    return int((counts > 0).sum()), int(counts.max())
 
-    weight_bytes = acc.expert_weight_bytes(wl.H, wl.F, touched)
-    flush = weight_bytes < 2 * L2_BYTES
+
+def time_forward(moe, wl, d, ws, K, warmup, world, dev, sample_clocks, local=0):
+    """K plain moe_forward steps after `warmup` untimed ones.  With weights that
+    fit in L2 the L2 is flushed before every step and each step is bracketed
+    by its own events, so the flush is not counted.  Returns (ms per step over
+    the slowest rank, clocks summary or None, flush)."""
+    touched, _ = routing_stats(moe, wl, d, ws)
+    flush = acc.expert_weight_bytes(wl.H, wl.F, touched) < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    args = (d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k)
 
     def barrier():
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize(dev)
-
-    nst = moe.FORWARD_STAGES
-    for _ in range(args.warmup):
-        moe.moe_forward(x, logits, W1, W3, W2, wl.k, out=out, ws=ws)
+    for _ in range(warmup):
+        moe.moe_forward(*args, out=out, ws=ws)
     st = moe.moe_get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {moe.moe_status_string(st)}")
-
-    # Timed region 1 (the value): K plain moe_forward steps.  With the L2 flush
-    # between steps, each step is bracketed by its own pair of events so the
-    # flush is not counted.
-    K = args.steps
     step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local) if rank == 0 else None
+    clocks = ClockSampler(local) if sample_clocks else None
     barrier()
     if clocks:
         time.sleep(0.3)
@@ -256,7 +281,7 @@ def bench_ours(args, rank, world, local):
         if flush:
             flush_buf.zero_()
             step_evs[i][0].record()
-        moe.moe_forward(x, logits, W1, W3, W2, wl.k, out=out, ws=ws)
+        moe.moe_forward(*args, out=out, ws=ws)
         if flush:
             step_evs[i][1].record()
     t_end.record()
@@ -269,66 +294,41 @@ def bench_ours(args, rank, world, local):
     region_ms = (sum(e[0].elapsed_time(e[1]) for e in step_evs) if flush
                  else t_start.elapsed_time(t_end))
     region_ms = max_over_ranks(region_ms, world, dev)
-    ms_per_step = region_ms / K
-    value = throughput(world, wl.T, K, region_ms)
+    return region_ms / K, (clocks.summary() if clocks else None), flush
 
-    # Timed region 2 (the per-kernel breakdown): K steps of moe_forward_events,
-    # one event between consecutive kernels on the launch stream.  The events
-    # themselves cost a few microseconds per step, which is why the value
-    # above comes from the region without them.
+
+def time_stages(moe, wl, d, ws, K, dev, flush):
+    """K moe_forward_events steps: each kernel's mean duration, from one CUDA
+    event between consecutive kernels on the launch stream."""
+    nst = moe.FORWARD_STAGES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
-    barrier()
+    torch.cuda.synchronize(dev)
     for i in range(K):
         if flush:
             flush_buf.zero_()
-        moe.moe_forward_events(x, logits, W1, W3, W2, wl.k, evs[i], out=out, ws=ws)
-    barrier()
-    stage_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j in range(nst)]
-    events_ms_per_step = statistics.fmean(evs[i][0].elapsed_time(evs[i][nst]) for i in range(K))
-
-    # end to end: host activations in, host result out, through the C ABI
-    e2e = None
-    if not args.no_e2e:
-        xh = x.cpu().pin_memory()
-        lh = logits.cpu().pin_memory()
-        oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
-        for _ in range(max(3, args.warmup // 2)):
-            moe.moe_forward_host(xh, lh, W1, W3, W2, wl.k, out_host=oh, ws=ws)
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(K):
-            if flush:
-                flush_buf.zero_()
-            moe.moe_forward_host(xh, lh, W1, W3, W2, wl.k, out_host=oh, ws=ws)
-        e1.record()
-        barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        e2e = {"value": throughput(world, wl.T, K, e2e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
-               "d2h_bytes_per_step": wl.T * wl.H * 2,
-               "ms_per_step": e2e_ms / K,
-               "note": "moe_forward_host on pinned host buffers: x and the logits are read and "
-                       "the result written across the host link by the kernels (each byte "
-                       "once), inside the timed region" + (", L2 flushed between steps"
-                                                           if flush else "")}
-
-    if rank != 0:
-        return None
-
-    peaks, peak_src = load_peaks()
+        moe.moe_forward_events(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k, evs[i],
+                               out=out, ws=ws)
+    torch.cuda.synchronize(dev)
     names = [moe.moe_forward_stage_name(j) for j in range(nst)]
-    mean_ms = {n: statistics.fmean(v) for n, v in zip(names, stage_ms)}
-    kern_sum = sum(mean_ms.values())
-    kernels = {n: {"ms": round(mean_ms[n], 5), "share": round(mean_ms[n] / kern_sum, 4)}
-               for n in names}
-    # roofline of the dominant kernel
-    top = max(mean_ms, key=mean_ms.get)
+    mean_ms = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+               for j, n in enumerate(names)}
+    per_step = statistics.fmean(evs[i][0].elapsed_time(evs[i][nst]) for i in range(K))
+    return mean_ms, per_step
+
+
+def kernel_roofline(wl, mean_ms, touched, peaks, peak_src, kernel=None):
+    """The roofline of one kernel (the dominant one unless named): algorithmic
+    bytes or FLOPs of a launch over its mean duration, against the measured
+    copy bandwidth or the sustained bf16 rate, whichever bounds it."""
+    P = wl.T * wl.k
+    top = kernel or max(mean_ms, key=mean_ms.get)
     kbytes = {"route": acc.route_bytes(wl.T, wl.E, wl.k),
               "scan": 0, "scatter": 4 * P * 4,
-              "gather": acc.gather_bytes(wl.T, wl.k, wl.H),
-              "fc1": acc.fc1_bytes(wl.H, wl.F, touched, P),
+              "gather": 0 if acc.ffn_gathers_rows(wl.T, wl.k, wl.E) else
+              acc.gather_bytes(wl.T, wl.k, wl.H),
+              "fc1": acc.fc1_bytes(wl.H, wl.F, touched, wl.T, wl.k, wl.E),
               "fc2": acc.fc2_bytes(wl.H, wl.F, touched, P),
               "combine": acc.combine_bytes(wl.T, wl.H, wl.k)}
     kflops = {"fc1": 2 * P * wl.H * 2 * wl.F, "fc2": 2 * P * wl.F * wl.H}
@@ -349,16 +349,83 @@ def bench_ours(args, rank, world, local):
     roof.update({"traffic": measured_traffic(wl.name, top), "kernel": top,
                  "algorithmic_bytes": kbytes.get(top), "algorithmic_flops": kflops.get(top),
                  "kernel_ms": round(mean_ms[top], 5), "peak_source": peak_note})
+    if roof["frac"] > 1.0:
+        roof["above_peak"] = ("the denominator is a measured copy (read + write streams); a "
+                              "read-dominated kernel can run above it")
+    return roof
 
+
+def layer_roofline(wl, ms_per_step, touched, peaks):
     flops = acc.ffn_flops(wl.T, wl.H, wl.F, wl.k)
     lbytes = acc.layer_bytes(wl.T, wl.H, wl.F, wl.E, wl.k, touched)
     t_roof, bound = acc.roofline_seconds(flops, lbytes, peaks["bf16_tflops"] * 1e12,
                                          peaks["hbm_gbs"] * 1e9)
-    layer = {"flops": flops, "bytes": lbytes, "t_roof_ms": round(t_roof * 1e3, 4),
-             "bound": bound, "frac": round(t_roof / (ms_per_step / 1e3), 4),
-             "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
-             "hbm_gbs": round(lbytes / (ms_per_step / 1e3) / 1e9, 1)}
+    return {"flops": flops, "bytes": lbytes, "t_roof_ms": round(t_roof * 1e3, 4),
+            "bound": bound, "frac": round(t_roof / (ms_per_step / 1e3), 4),
+            "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
+            "hbm_gbs": round(lbytes / (ms_per_step / 1e3) / 1e9, 1)}
 
+
+def bench_ours(args, rank, world, local):
+    import routing_grouped_expert_gb300 as moe
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[args.workload]
+    pool = Inputs(dev)
+    d = pool.get(wl)
+    ws = moe.Workspace(dev)
+    touched, max_count = routing_stats(moe, wl, d, ws)
+    weight_bytes = acc.expert_weight_bytes(wl.H, wl.F, touched)
+    P = wl.T * wl.k
+    K = args.steps
+
+    # the value: K plain moe_forward steps
+    ms_per_step, clocks, flush = time_forward(moe, wl, d, ws, K, args.warmup, world, dev,
+                                              rank == 0, local)
+    value = throughput(world, wl.T, K, ms_per_step * K)
+    # the per-kernel breakdown: a second region with stage events
+    mean_ms, events_ms_per_step = time_stages(moe, wl, d, ws, K, dev, flush)
+
+    # end to end: host activations in, host result out, through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        xh = d["x"].cpu().pin_memory()
+        lh = d["logits"].cpu().pin_memory()
+        oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        flush_buf = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+                     if flush else None)
+        for _ in range(max(3, args.warmup // 2)):
+            moe.moe_forward_host(xh, lh, d["W1"], d["W3"], d["W2"], wl.k, out_host=oh, ws=ws)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            if flush:
+                flush_buf.zero_()
+            moe.moe_forward_host(xh, lh, d["W1"], d["W3"], d["W2"], wl.k, out_host=oh, ws=ws)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": throughput(world, wl.T, K, e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
+               "d2h_bytes_per_step": wl.T * wl.H * 2,
+               "ms_per_step": e2e_ms / K,
+               "note": "moe_forward_host on pinned host buffers: x and the logits are read and "
+                       "the result written across the host link by the kernels (each byte "
+                       "once), inside the timed region" + (", L2 flushed between steps"
+                                                           if flush else "")}
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    kern_sum = sum(mean_ms.values())
+    kernels = {n: {"ms": round(v, 5), "share": round(v / kern_sum, 4)} for n, v in mean_ms.items()}
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -371,18 +438,107 @@ def bench_ours(args, rank, world, local):
                    f"streamed per step)"),
             "touched_experts": touched, "max_expert_count": max_count,
             "mean_expert_count": P / wl.E}),
-        "roofline": roof,
-        "layer_roofline": layer,
+        "roofline": kernel_roofline(wl, mean_ms, touched, peaks, peak_src),
+        "layer_roofline": layer_roofline(wl, ms_per_step, touched, peaks),
         "kernels": kernels,
         "kernels_timing": ("per-stage CUDA events on the launch stream, in a second timed "
                            f"region of {K} moe_forward_events steps "
                            f"({events_ms_per_step:.4f} ms per step with the events)"),
-        "gpu_launches": nst * K,
-        "clocks": clocks.summary() if clocks else None,
+        "gpu_launches": moe.FORWARD_STAGES * K,
+        "clocks": clocks,
     }
     if e2e:
         result["e2e"] = e2e
-    return result, d, counts
+    if world == 1 and not args.no_configs:
+        result["configs"] = bench_configs(moe, args, pool, ws, dev, wl.name, ms_per_step)
+    if world == 1 and not args.no_protocol:
+        result["protocol"] = bench_protocol(moe, args, pool, ws, dev, wl, ms_per_step)
+    return result, d
+
+
+def bench_configs(moe, args, pool, ws, dev, main_name, main_ms):
+    """Every other workload of record, measured in this process: time per
+    step, the layer's roofline fraction, the dominant kernel's roofline and
+    the clocks of its timed region; the skewed workloads also as a ratio to
+    the uniform fine-grained time."""
+    peaks, peak_src = load_peaks()
+    out = {}
+    times = {main_name: main_ms}
+    for name in OTHER_CONFIGS:
+        if name == main_name:
+            continue
+        wl = I.WORKLOADS[name]
+        d = pool.get(wl)
+        touched, max_count = routing_stats(moe, wl, d, ws)
+        K = max(10, args.steps)
+        ms, clocks, flush = time_forward(moe, wl, d, ws, K, max(3, args.warmup), 1, dev, True)
+        mean_ms, _ = time_stages(moe, wl, d, ws, K, dev, flush)
+        times[name] = ms
+        lay = layer_roofline(wl, ms, touched, peaks)
+        roof = kernel_roofline(wl, mean_ms, touched, peaks, peak_src)
+        out[name] = {"T": wl.T, "H": wl.H, "F": wl.F, "E": wl.E, "k": wl.k,
+                     "ms_per_step": round(ms, 5), "tokens_per_s": round(wl.T / ms * 1e3, 1),
+                     "layer_frac": lay["frac"], "layer_bound": lay["bound"],
+                     "layer_tflops": lay["tflops"],
+                     "kernel": roof["kernel"], "kernel_frac": roof["frac"],
+                     "kernel_bound": roof["bound"], "kernel_ms": roof["kernel_ms"],
+                     "touched_experts": touched, "max_expert_count": max_count,
+                     "l2": "flushed between steps" if flush else "inputs larger than L2",
+                     "steps": K, "clocks": clocks}
+        del d
+    if "fine_grained" in times:
+        for name in ("skewed", "skewed_10x"):
+            if name in out:
+                out[name]["ratio_to_fine_grained"] = round(times[name] / times["fine_grained"], 4)
+    return out
+
+
+def bench_protocol(moe, args, pool, ws, dev, wl, main_ms):
+    """The headline as a median: the workload's time per step on three
+    realizations of its inputs (seeds shifted by 1000 r), measured here and in a
+    second, fresh process; reports the median and the spread of the six."""
+    K = max(10, args.steps)
+    here = []
+    for r in range(3):
+        w = wl.with_(realization=r)
+        d = pool.get(w)
+        ms, _, _ = time_forward(moe, w, d, ws, K, max(3, args.warmup), 1, dev, False)
+        here.append(ms)
+        del d
+    pool.weights = {k: v for k, v in pool.weights.items() if k[3] == 0}
+    torch.cuda.empty_cache()
+    cmd = [sys.executable, os.path.abspath(__file__), "--protocol-child", "--workload", wl.name,
+           "--steps", str(K), "--warmup", str(max(3, args.warmup))]
+    there = []
+    try:
+        res = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        there = json.loads(res.stdout.strip().splitlines()[-1])["ms"] if res.returncode == 0 else []
+    except (subprocess.TimeoutExpired, ValueError, IndexError, KeyError):
+        there = []
+    allv = here + there
+    return {"ms_per_step_median": round(statistics.median(allv), 5),
+            "ms_per_step_min": round(min(allv), 5), "ms_per_step_max": round(max(allv), 5),
+            "spread": round((max(allv) - min(allv)) / statistics.median(allv), 4),
+            "this_process_ms": [round(v, 5) for v in here],
+            "fresh_process_ms": [round(v, 5) for v in there],
+            "how": f"{K} timed steps per realization; realizations r = 0, 1, 2 (seeds + 1000 r) "
+                   "in this process and again in a fresh process"}
+
+
+def protocol_child(args):
+    import routing_grouped_expert_gb300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[args.workload]
+    pool = Inputs(dev)
+    ws = moe.Workspace(dev)
+    ms = []
+    for r in range(3):
+        w = wl.with_(realization=r)
+        d = pool.get(w)
+        ms.append(time_forward(moe, w, d, ws, args.steps, args.warmup, 1, dev, False)[0])
+        del d
+    print(json.dumps({"ms": ms}), flush=True)
 
 
 # ------------------------------------------------------- the CPU oracle
@@ -399,7 +555,7 @@ class _ExpertCache(dict):
         return a
 
 
-def oracle_sampler(wl, d, mem_cap=24 * 2**30, max_pool=64):
+def oracle_sampler(wl, d, mem_cap=12 * 2**30, max_pool=64):
     """A pool of the batch's first tokens whose experts' fp64 weights fit in
     `mem_cap`, and a function that runs the oracle on n of them."""
     from oracle import moe_oracle as O
@@ -511,8 +667,10 @@ def bench_sweep(args):
         torch.cuda.synchronize(dev)
         if moe.moe_get_device_status(ws) != 0:
             raise RuntimeError("device status after sweep point")
+        names = [moe.moe_forward_stage_name(j) for j in range(nst)]
+        f1, f2 = names.index("fc1"), names.index("fc2") + 1
         step = statistics.median(evs[i][0].elapsed_time(evs[i][nst]) for i in range(K))
-        ffn = statistics.median(evs[i][4].elapsed_time(evs[i][6]) for i in range(K))
+        ffn = statistics.median(evs[i][f1].elapsed_time(evs[i][f2]) for i in range(K))
         flops = acc.ffn_flops(T, base.H, base.F, base.k)
         util = acc.util(base.k, base.E, peaks["hbm_gbs"] * 1e9, peaks["bf16_tflops"] * 1e12, T)
         points.append({"tokens_per_expert": be, "T": T, "layer_ms": round(step, 5),
@@ -591,6 +749,51 @@ def bench_gated(args):
                                "peak_source": peak_src}}
 
 
+# ------------------------------------------------- feature-sharded layer
+def bench_shard(args, rank, world, local):
+    """The layer split over `world` ranks along the FFN features: every rank
+    routes all T tokens and computes its slice's fp32 partial output; one
+    all-reduce sums them and the sum is rounded once.  Strong scaling: the
+    job's work per step is one layer of T tokens whatever the rank count."""
+    import routing_grouped_expert_gb300 as moe
+    from routing_grouped_expert_gb300 import sharded
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[args.workload]
+    W1, W3, W2 = I.make_weights(wl, dev)
+    W1s, W3s, W2s = sharded.shard_weights(W1, W3, W2, world, rank)
+    del W1, W3, W2
+    torch.cuda.empty_cache()
+    x, logits = I.make_x(wl, dev), I.make_logits(wl).to(dev)
+    ws = moe.Workspace(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        sharded.sharded_forward(x, logits, W1s, W3s, W2s, wl.k, ws=ws)
+    if moe.moe_get_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record()
+    for _ in range(args.steps):
+        sharded.sharded_forward(x, logits, W1s, W3s, W2s, wl.k, ws=ws)
+    e1.record()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    if rank != 0:
+        return None
+    return {"metric": METRIC, "mode": "shard_f", "value": round(wl.T / (ms / 1e3), 1),
+            "unit": UNIT, "n_gpus": world, "ms_per_step": round(ms, 5), "steps": args.steps,
+            "warmup": args.warmup, "scaling": "strong", "dtype": "bf16", "data": "synthetic",
+            "config": wl_config(wl, {"parallelism": f"FFN features split over {world} "
+                                                    f"rank(s), one fp32 all-reduce",
+                                     "F_per_rank": W1s.shape[2]})}
+
+
 # --------------------------------------------------------- training step
 def bench_train(args):
     """moe_forward_train then moe_backward on the workload, dout ~ N(0, 1).
@@ -640,6 +843,9 @@ def bench_train(args):
 
 def main():
     args = parse()
+    if args.protocol_child:
+        protocol_child(args)
+        return
     if args.train:
         print(json.dumps(bench_train(args)), flush=True)
         return
@@ -655,14 +861,18 @@ def main():
         if torch.cuda.is_available():
             torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    if args.impl == "reference":
+    if args.shard_f:
+        res = bench_shard(args, rank, world, local)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+    elif args.impl == "reference":
         res = bench_reference(args, rank, world, local)
         if res is not None:
             print(json.dumps(res), flush=True)
     else:
         out = bench_ours(args, rank, world, local)
         if out is not None:
-            res, d, _ = out
+            res, d = out
             if world == 1 and not args.no_cpu_baseline:
                 wl = I.WORKLOADS[args.workload]
                 res["cpu_baseline"] = cpu_baseline(wl, d)

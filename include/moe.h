@@ -91,8 +91,12 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k,
  *   sorted_src [T*k]  int32 out: sorted_src[p] = a, p ascending within each
  *              expert's range [offsets[e], offsets[e+1]) in ascending a.
  *   dest_of    [T*k]  int32 out: inverse map, sorted_src[dest_of[a]] == a.
- * Deterministic: bit-identical on every run.  An out-of-range expert index
- * gives MOE_ERR_INVALID_ARG in the device status and unspecified outputs.
+ * Deterministic: bit-identical on every run.  An expert index outside
+ * [0, E) sets MOE_ERR_INVALID_ARG in the device status; that assignment is
+ * left out of the counts and takes no position: its dest_of is -1, and
+ * sorted_src[offsets[E] .. T*k) holds -1.  The other assignments are grouped
+ * as above.  moe_grouped_ffn and moe_combine skip positions and slots marked
+ * -1, so a bad index never turns into a memory access.
  */
 moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k,
                        int32_t* counts, int32_t* offsets,
@@ -103,11 +107,19 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k,
  * Step 3 -- per-expert SwiGLU FFN as a grouped GEMM over the expert groups
  * ("Piper", §III-A: W_gate, W_up in R^{d x dffn}, W_down in R^{dffn x d};
  * "MegaScale-Infer", §3.4 Performance Simulation Model: FFN Input and FFN
- * Output GEMMs; tile-aligned token blocks of at most 128 rows per expert,
- * at most one partial block per expert: "MegaFlux", §3.1).
+ * Output GEMMs; token blocks of at most beta rows per expert: "MegaFlux",
+ * §3.1).  beta is 64, 128 or 256 rows, chosen from the mean rows per expert
+ * (T*k/E at most 40, at most 80, above); an expert's rows are cut into
+ * ceil(rows / beta) blocks of equal size (a multiple of 16 rows), so no block
+ * is a near-empty tail.  The groups are unpadded: nothing is stored for rows
+ * past offsets[E].
  *
  *   x          [T, H] bf16.
- *   sorted_src [T*k], offsets [E+1] as produced by moe_permute.
+ *   sorted_src [T*k], offsets [E+1] as produced by moe_permute (positions
+ *              holding -1 are skipped).  offsets that do not group T*k rows
+ *              (offsets[0] != 0, a decrease, offsets[E] > T*k) set
+ *              MOE_ERR_INVALID_ARG in the device status and nothing is
+ *              computed.
  *   W1, W3     [E, H, F] bf16: gate (silu applied) and up projections.
  *   W2         [E, F, H] bf16: down projection.
  *   y_sorted   [T*k, H] bf16 out: y_sorted[p] = FFN_e(x[sorted_src[p]/k])
@@ -128,7 +140,9 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src,
  *   out[t] = sum_{j<k} topk_w[t,j] * y_sorted[dest_of[t*k+j]], summed in
  *   slot order in fp32 and rounded once to bf16.
  *   y_sorted [T*k, H] bf16, dest_of [T*k] int32, topk_w [T, k] fp32,
- *   out [T, H] bf16 out.  No workspace.
+ *   out [T, H] bf16 out.  No workspace.  A slot whose dest_of is outside
+ *   [0, T*k) (-1 from moe_permute for an out-of-range expert index) adds
+ *   nothing.
  */
 moe_status moe_combine(const void* y_sorted, const int32_t* dest_of,
                        const float* topk_w, int T, int H, int k,
@@ -158,15 +172,18 @@ moe_status moe_combine(const void* y_sorted, const int32_t* dest_of,
  * and NB = ceil(T*k / 128) + min(T*k, E) token blocks -- for example
  * T = 8192, k = 8, E = 256 needs about 136 KB.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture begins.  Every call shares the one array and
- * it keeps the previous call's contents (the status word is cleared by
- * each call), so calls whose work overlaps on the GPU -- on different
- * streams, or from different threads -- race and corrupt each other's
- * results; serialise them.  Out-of-range expert indices are skipped (the
- * outputs are then unspecified) but, unlike moe_permute, cannot be read
- * back as a device status.
+ * The first call in each CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) with that context current, and caches it under the
+ * context's ID; make that first call before any stream capture begins.  A
+ * device reset (or a new context on the same device) loads the library's
+ * device code afresh, at an address of its own: the next call sees a new
+ * context ID and looks the address up again, so it never uses a stale one.
+ * Every call shares the one array and it keeps the previous call's contents
+ * (the status word is cleared by each call), so calls whose work overlaps on
+ * the GPU -- on different streams, or from different threads -- race and
+ * corrupt each other's results; serialise them.  Out-of-range expert indices
+ * get the same -1 markers as in moe_permute (so the gather and the combine
+ * skip them) but, unlike moe_permute, cannot be read back as a device status.
  */
 #define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
 moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int E, int k,
@@ -184,6 +201,27 @@ moe_status moe_forward(const void* x, const float* router_logits,
                        const void* W1, const void* W3, const void* W2,
                        int T, int H, int F, int E, int k, void* out,
                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward with the combine's fp32 sum left unrounded: out [T, H] fp32.
+ * For a layer split over GPUs along the FFN features ("MegaScale-Infer",
+ * §3.4 Performance Simulation Model: expert tensor parallelism, tpe), where
+ * each GPU holds W1[:, :, Fg], W3[:, :, Fg] and W2[:, Fg, :] for its slice
+ * Fg of the features, routes every token identically and computes this
+ * partial output; the sum of the partials over the GPUs (one all-reduce or
+ * reduce-scatter, in fp32) is the layer, since SwiGLU acts feature by
+ * feature and the combine is linear.  Same arguments, workspace and status
+ * as moe_forward; F is the slice's width (a multiple of 128).
+ */
+moe_status moe_forward_f32(const void* x, const float* router_logits,
+                           const void* W1, const void* W3, const void* W2,
+                           int T, int H, int F, int E, int k, float* out,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* out[i] = bf16(in[i]) for i < n, round to nearest even: the layer's output
+ * from the reduced fp32 partials of moe_forward_f32.  in fp32 [n], out bf16
+ * [n], both 16-byte aligned device pointers; no workspace. */
+moe_status moe_cast_bf16(const float* in, void* out, size_t n, void* stream);
 
 /*
  * The whole layer with the per-step activations in HOST memory: takes
@@ -269,7 +307,9 @@ moe_status moe_backward(const void* dout, const float* router_logits,
 /*
  * moe_forward with timing marks: records events[0] on `stream` before the
  * first kernel and events[i] after stage i, for the MOE_FORWARD_STAGES
- * stages route, scan, scatter, gather, fc1, fc2, combine (in that order).
+ * stages route, scan, scatter, gather, fc1, fc2, combine (in that order; the
+ * gather stage is empty when the token blocks are small -- T*k <= 40 E -- and
+ * FC1 gathers the rows of x it needs itself).
  * `events` points to MOE_FORWARD_STAGES + 1 cudaEvent_t created by the
  * caller.  Same arguments, work and results as moe_forward.
  */
@@ -282,6 +322,55 @@ moe_status moe_forward_events(const void* x, const float* router_logits,
 
 /* Name of timing stage i of moe_forward_events (NULL if out of range). */
 const char* moe_forward_stage_name(int i);
+
+/*
+ * Expert-replica planning for expert-parallel execution on G GPUs
+ * ("MegaFlux: Skew-Resilient MoE Megakernels via Pipelined Expert
+ * Replication", §3.1 Planner: replica placement and token-block assignment;
+ * §A.1 Greedy placement and refinement; §A.2 Reduction-aware planning).
+ * Runs on the device, from the per-expert row counts of a routing (e.g. the
+ * `counts` of moe_permute), so no host round trip sits between routing and
+ * the plan; it changes no routed assignment, only which GPU computes which
+ * token blocks of an expert.
+ *
+ * GPU g owns experts [ceil(g E / G), ceil((g+1) E / G)), i.e. expert e is owned
+ * by floor(e G / E).  Each expert's rows are cut into ceil(c_e / beta) blocks
+ * (the last one partial); block counts are the load.  Starting from the
+ * no-replica plan, four bounded greedy searches move blocks from GPUs above
+ * tau = ceil(total blocks / G) to GPUs below it that hold the expert, or to a
+ * new replica there (at most `budget` replicas per GPU), for at most s + 2
+ * rounds (s = `rounds`, or the budget when `rounds` is -1); the plan with the
+ * smallest maximum load (then fewest replicas) is refined -- redundant
+ * replicas pruned, single blocks moved between holders of an expert -- and,
+ * when lambda >= 0 (backward plans, lambda = 12 in the pages), pruned with a
+ * penalty of lambda blocks per remote replica charged to the expert's owner,
+ * falling back to the no-replica plan unless that lowers the penalised
+ * maximum load.  Ties go to the lower GPU, then the lower expert: the plan is
+ * a deterministic function of the counts.
+ *
+ *   counts         [E] int32 device in: routed rows per expert (>= 0).
+ *   blocks_per_gpu [E, G] int32 out: blocks of expert e computed on GPU g
+ *                  (row sums = ceil(c_e / beta)).
+ *   row_ranges     [E, G, 2] int32 out: [lo, hi) of expert e's rows (offsets
+ *                  inside its group, routed order) that GPU g computes; the
+ *                  holders take consecutive ranges in ascending GPU order.
+ *   gpu_load       [G] int32 out: blocks per GPU.
+ *   info           [4] int32 out: the winning search (0-3: donor priority by
+ *                  GPU load / by block count x one / several new replicas
+ *                  per round; 4: the no-replica plan), tau, the number of
+ *                  replicas, the maximum load.
+ *   ws             moe_plan_workspace_size(E, G) bytes, 256-byte aligned.
+ * Limits: 1 <= G <= min(E, MOE_PLAN_MAX_GPUS), E <= MOE_MAX_EXPERTS,
+ * beta >= 1, 0 <= budget <= E, rounds >= -1, lambda >= -1; otherwise
+ * MOE_ERR_INVALID_ARG with nothing enqueued.  One CTA of 128 threads; its
+ * time grows with E * G and with the number of single-block moves.
+ */
+#define MOE_PLAN_MAX_GPUS 64
+size_t moe_plan_workspace_size(int E, int G);
+moe_status moe_plan_replicas(const int32_t* counts, int E, int G, int beta, int budget,
+                             int rounds, int lambda, int32_t* blocks_per_gpu,
+                             int32_t* row_ranges, int32_t* gpu_load, int32_t* info,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Synchronises `stream` and returns the device status word of `ws`

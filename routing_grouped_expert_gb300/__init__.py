@@ -12,6 +12,8 @@ from .binding import (  # noqa: F401
     moe_diag_wait_timeout,
     moe_forward,
     moe_forward_events,
+    moe_forward_f32,
+    moe_cast_bf16,
     moe_forward_stage_name,
     FORWARD_STAGES,
     moe_forward_host,
@@ -24,6 +26,8 @@ from .binding import (  # noqa: F401
     moe_get_device_status,
     moe_grouped_ffn,
     moe_permute,
+    moe_plan_replicas,
+    moe_plan_workspace_size,
     moe_route_topk,
     moe_status_string,
     moe_workspace_size,

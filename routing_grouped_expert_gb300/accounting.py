@@ -71,9 +71,19 @@ def gather_bytes(T: int, k: int, H: int) -> int:
     return T * H * BF16 + T * k * H * BF16 + T * k * INT32
 
 
-def fc1_bytes(H: int, F: int, touched: int, P: int) -> int:
-    """W1 and W3 of touched experts + gathered x rows read + h written."""
-    return 2 * H * F * BF16 * touched + P * H * BF16 + P * F * BF16
+def ffn_gathers_rows(T: int, k: int, E: int) -> bool:
+    """Whether FC1 gathers its token rows from x itself (the library does so
+    when the mean rows per expert T*k/E is at most 40, its smallest block
+    size); otherwise the gather kernel writes them in expert order first."""
+    return T * k <= 40 * E
+
+
+def fc1_bytes(H: int, F: int, touched: int, T: int, k: int, E: int) -> int:
+    """W1 and W3 of touched experts + the token rows read + h written.  The
+    rows are x itself (each of its T rows read once from HBM) when FC1
+    gathers them, else the T*k rows of the expert-ordered copy."""
+    rows = T if ffn_gathers_rows(T, k, E) else T * k
+    return 2 * H * F * BF16 * touched + rows * H * BF16 + T * k * F * BF16
 
 
 def fc2_bytes(H: int, F: int, touched: int, P: int) -> int:

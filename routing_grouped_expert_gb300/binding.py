@@ -45,6 +45,10 @@ SIGNATURES = {
     "moe_workspace_size_gated": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_gated": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                                _VP, _VP, _SZ, _VP]),
+    "moe_forward_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_cast_bf16": (_I, [_VP, _VP, _SZ, _VP]),
+    "moe_plan_workspace_size": (_SZ, [_I, _I]),
+    "moe_plan_replicas": (_I, [_VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
 }
 
 
@@ -238,6 +242,35 @@ def moe_forward(x, router_logits, W1, W3, W2, k: int, out=None, ws: Workspace | 
 FORWARD_STAGES = 7
 
 
+def moe_forward_f32(x, router_logits, W1, W3, W2, k: int, out=None,
+                    ws: Workspace | None = None):
+    """The layer with its fp32 combine sum unrounded ([T, H] fp32): a partial
+    output of a layer split over GPUs along the FFN features."""
+    T, H = x.shape
+    E, _, F = W1.shape
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_logits, torch.float32, (T, E), "router_logits")
+    _need(W1, torch.bfloat16, (E, H, F), "W1")
+    _need(W3, torch.bfloat16, (E, H, F), "W3")
+    _need(W2, torch.bfloat16, (E, F, H), "W2")
+    out = torch.empty(T, H, dtype=torch.float32, device=x.device) if out is None else out
+    _need(out, torch.float32, (T, H), "out")
+    ws = _ws(ws, moe_workspace_size(T, H, F, E, k))
+    _check(load_library().moe_forward_f32(_p(x), _p(router_logits), _p(W1), _p(W3), _p(W2), T,
+                                          H, F, E, k, _p(out), ws.ptr, ws.nbytes, _stream()),
+           "moe_forward_f32")
+    return out
+
+
+def moe_cast_bf16(x: torch.Tensor, out=None):
+    """bf16 copy of an fp32 tensor (round to nearest even), on the GPU."""
+    _need(x, torch.float32, tuple(x.shape), "x")
+    out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out, torch.bfloat16, tuple(x.shape), "out")
+    _check(load_library().moe_cast_bf16(_p(x), _p(out), x.numel(), _stream()), "moe_cast_bf16")
+    return out
+
+
 def moe_forward_stage_name(i: int) -> str:
     r = load_library().moe_forward_stage_name(i)
     return None if r is None else r.decode()
@@ -370,3 +403,27 @@ def moe_backward(dout, router_logits, W1, W3, W2, k: int, ws: Workspace):
                                        F, E, k, _p(dx), _p(dl), _p(dW1), _p(dW3), _p(dW2),
                                        ws.ptr, ws.nbytes, _stream()), "moe_backward")
     return dx, dl, dW1, dW3, dW2
+
+
+def moe_plan_workspace_size(E: int, G: int) -> int:
+    return load_library().moe_plan_workspace_size(E, G)
+
+
+def moe_plan_replicas(counts: torch.Tensor, G: int, beta: int, budget: int, rounds: int = -1,
+                      lam: int = -1, ws: Workspace | None = None):
+    """Replica plan of expert row counts [E] (int32, on the GPU) for G GPUs.
+    Returns (blocks_per_gpu [E, G], row_ranges [E, G, 2], gpu_load [G], info [4]),
+    int32 tensors on the counts' device; lam = -1: no reduction penalty."""
+    E = counts.shape[0]
+    _need(counts, torch.int32, (E,), "counts")
+    dev = counts.device
+    n = torch.empty(E, G, dtype=torch.int32, device=dev)
+    rows = torch.empty(E, G, 2, dtype=torch.int32, device=dev)
+    load = torch.empty(G, dtype=torch.int32, device=dev)
+    info = torch.empty(4, dtype=torch.int32, device=dev)
+    need = moe_plan_workspace_size(E, G)
+    ws = _ws(ws, max(need, 256))
+    _check(load_library().moe_plan_replicas(_p(counts), E, G, beta, budget, rounds, lam, _p(n),
+                                            _p(rows), _p(load), _p(info), ws.ptr, ws.nbytes,
+                                            _stream()), "moe_plan_replicas")
+    return n, rows, load, info

@@ -94,8 +94,8 @@ cudaError_t launch_single_expert_plan(int T, int beta, const SingleExpertPlan& p
   single_expert_offsets_kernel<<<1, 1, 0, s>>>(plan.offsets, T);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  return launch_plan(plan.offsets, 1, plan.block_off, plan.num_blocks, plan.block_expert, beta,
-                     s);
+  return launch_plan(plan.offsets, 1, T, plan.block_off, plan.num_blocks, plan.block_expert,
+                     beta, nullptr, s);
 }
 
 }  // namespace moe

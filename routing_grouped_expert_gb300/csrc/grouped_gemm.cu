@@ -44,10 +44,7 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = kTileM;          // weight rows (output features) per MMA (M)
-constexpr int BK = kTileK;          // K per pipeline stage
-constexpr int kAHalfBytes = 64 * BK * 2;          // one 64-feature TMA box: 8 KB
-constexpr int kABytes = BM * BK * 2;              // 16 KB per weight tile per stage
-constexpr int kBBoxBytes = kRowBox * BK * 2;      // 32 token rows: 4 KB
+constexpr int BK = kTileK;          // K per pipeline stage (the default; see Cfg::kBK)
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 204800;               // operand ring: at most 200 KB
@@ -75,7 +72,12 @@ template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false,
           bool kDualK = false>
 struct Cfg {
   static constexpr bool kGLU = kEpi == kEpiSwiglu || kEpi == kEpiSwigluSave;
-  static constexpr int kBBytes = kBN * BK * 2;
+  static constexpr int kBK = BK;
+  static constexpr int kAHalfBytes = 64 * kBK * 2;      // one 64-feature atom of a weight tile
+  static constexpr int kABytes = BM * kBK * 2;          // one 128-feature weight tile
+  static constexpr int kRowBytes = kBK * 2;             // one token row of the N operand
+  static constexpr int kBBoxBytes = kRowBox * kRowBytes;   // 32 token rows
+  static constexpr int kBBytes = kBN * kRowBytes;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
   // bf16 outputs per accumulator column: each leaves through a 16-row x
   // 32-feature staging box (1 KB per warp) and a TMA store
@@ -247,6 +249,19 @@ struct RowMaps {
   CUtensorMap m[2][4];
 };
 
+// Four rows (y0..y3) of 64 K each from a 2-D tensor map whose box is one row
+// high, stored as consecutive 128-byte rows at dst (the map's swizzle applied).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y0, int y1, int y2, int y3,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1),
+      "r"(y2), "r"(y3), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
                                              int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
@@ -269,7 +284,12 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK>
+// kGather: the token rows of the N operand are gathered straight from x
+// ([T, K], token-major) by TMA tile::gather4 loads -- row p of an expert
+// group is token sorted_src[p] / k -- so no expert-ordered copy of x is made
+// (FC1 of the forward).  rows.m[0][0] is then a tensor map of x with boxes of
+// one row x 64 K; the producer warp's lanes each gather four rows at a time.
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -278,8 +298,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ num_blocks_ptr,
                     const int32_t* __restrict__ block_expert, int n_mt, int K,
                     void* __restrict__ out_ptr, int ld_out, int m_valid, EpiAux aux,
-                    const __grid_constant__ OutMaps outs, StreamK sk, int* __restrict__ status) {
+                    const __grid_constant__ OutMaps outs, StreamK sk,
+                    const int32_t* __restrict__ gather_src, int gather_k,
+                    int* __restrict__ status) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  constexpr int kBK = C::kBK;
+  static_assert(!kGather || (!kDualK && !kAKMajor), "gathered rows: forward products only");
   constexpr bool kGLU = C::kGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -294,7 +318,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2;
   constexpr size_t kSlot = (size_t)kNumA * BM * kBN;   // floats of one partial tile
   const bool sk_ok = kSKCapable && sk.part != nullptr;
-  const int nkb = K / BK;                        // K stages per phase
+  const int nkb = K / kBK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
 
   if (threadIdx.x == 0) {
@@ -333,7 +357,124 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   const uint32_t tmem_base = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
 
-  if (warp == 0) {
+  if (warp == 0 && kGather) {
+    // ----------------------------------- TMA producer, gathered token rows
+    // Lane 0 draws the segments, waits for free stages and loads the weight
+    // tiles; every lane then gathers its share of the block's token rows
+    // (kRowsPerLane rows, four per instruction) into the same stage.
+    constexpr int kRowsPerLane = kBN / 32 < 4 ? 4 : kBN / 32;
+    const uint64_t pol_once = policy_evict_first();
+    const uint64_t pol_shared = policy_evict_normal();
+    const uint64_t pol_x = policy_evict_last();      // x rows: reused by every feature tile
+    const CUtensorMap* xmap = &rows.m[0][0];
+    int stage = 0, issued = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    // only lane 0 draws from the queue; the other lanes' copies stay idle
+    Segments sg(sk_ok, total, nkb_all, lane == 0 ? sk.queue : nullptr);
+    int sslot = 0;
+    uint32_t sphase = 0;
+    while (true) {
+      int w = 0, kb0 = 0, kb1 = 0, have = 0;
+      if (lane == 0 && ok) {
+        have = sg.next(w, kb0, kb1) ? 1 : 0;
+        // hand the segment to the MMA warp and the epilogue
+        if (have) {
+          if (mbar_wait(&bars->seg_empty[sslot], sphase ^ 1u, abort_flag, kWaitLimitNs)) {
+            bars->seg[sslot] = make_int4(w, kb0, kb1, 0);
+            mbar_arrive(&bars->seg_full[sslot]);
+            if (++sslot == kSegRing) {
+              sslot = 0;
+              sphase ^= 1u;
+            }
+          } else {
+            ok = false;
+            have = 0;
+          }
+        }
+      }
+      have = __shfl_sync(0xffffffffu, have, 0);
+      if (!have) break;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      kb0 = __shfl_sync(0xffffffffu, kb0, 0);
+      kb1 = __shfl_sync(0xffffffffu, kb1, 0);
+      const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
+      const int n16 = (it.nrows + 15) & ~15;        // rows the MMA reads
+      // this lane's token rows; rows past the block repeat its last row
+      int tok[kRowsPerLane];
+#pragma unroll
+      for (int i = 0; i < kRowsPerLane; ++i) {
+        const int r = min(lane * kRowsPerLane + i, it.nrows - 1);
+        tok[i] = __ldg(gather_src + it.row0 + r) / gather_k;
+      }
+      const uint32_t bytes = kNumA * C::kABytes + (uint32_t)n16 * C::kRowBytes;
+      const int f0 = it.mt * C::kFeatPerItem;
+      const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        int free_ok = 1;
+        if (lane == 0) {
+          free_ok = mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (free_ok) {
+            uint64_t* fb = &bars->full[stage];
+            uint8_t* sA = smem + stage * C::kStageBytes;
+            const int k0 = kb * kBK;
+            mbar_arrive_expect_tx(fb, bytes);
+#pragma unroll
+            for (int a = 0; a < kNumA; ++a) {
+              const CUtensorMap* map = (kGLU && a == 1) ? &tmA1 : &tmA0;
+              const int fa = f0 + (kGLU ? 0 : a * BM);
+              if (a_atoms) {
+                tma_load_4d(sA + a * C::kABytes, map, fb, 0, k0, fa >> 6, it.e, pol_w);
+              } else {
+                tma_load_3d(sA + a * C::kABytes, map, fb, fa, k0, it.e, pol_w);
+                tma_load_3d(sA + a * C::kABytes + C::kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
+              }
+            }
+          }
+        }
+        free_ok = __shfl_sync(0xffffffffu, free_ok, 0);
+        if (!free_ok) {
+          ok = false;
+          break;
+        }
+        // the expected bytes are posted before any row lands
+        uint64_t* fb = &bars->full[stage];
+        uint8_t* sB = smem + stage * C::kStageBytes + kNumA * C::kABytes;
+        const int k0 = kb * kBK;
+#pragma unroll
+        for (int g = 0; g < kRowsPerLane / 4; ++g) {
+          const int r0 = lane * kRowsPerLane + 4 * g;
+          if (r0 < n16)
+            tma_gather4(sB + r0 * C::kRowBytes, xmap, fb, k0, tok[4 * g], tok[4 * g + 1],
+                        tok[4 * g + 2], tok[4 * g + 3], pol_x);
+        }
+        ++issued;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+    }
+    if (lane == 0) {
+      if (ok) {   // no more segments
+        if (mbar_wait(&bars->seg_empty[sslot], sphase ^ 1u, abort_flag, kWaitLimitNs)) {
+          bars->seg[sslot] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&bars->seg_full[sslot]);
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailProducer);
+        *abort_flag = 1;
+      }
+      // No TMA write may land after the CTA exits: wait for the last loads.
+      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+        mbar_wait(&bars->full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), nullptr,
+                  kWaitLimitNs);
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       // Weights: a tile read by a single token block is streamed past L2
@@ -368,7 +509,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
         const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
-        const uint32_t bytes = kNumA * kABytes + nbox * kBBoxBytes;
+        const uint32_t bytes = kNumA * C::kABytes + nbox * C::kBBoxBytes;
         const int f0 = it.mt * C::kFeatPerItem;
         const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -377,9 +518,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             break;
           }
           const bool second = kDualK && kb >= nkb;    // second K phase
-          const int k0 = (second ? kb - nkb : kb) * BK;
+          const int k0 = (second ? kb - nkb : kb) * kBK;
           uint8_t* sA = smem + stage * C::kStageBytes;
-          uint8_t* sB = sA + kNumA * kABytes;
+          uint8_t* sB = sA + kNumA * C::kABytes;
           uint64_t* fb = &bars->full[stage];
           mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
@@ -388,15 +529,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             const int fa = f0 + (kGLU ? 0 : a * BM);
             if constexpr (kAKMajor) {
               // 128 weight rows x 64 K, K contiguous: one box
-              tma_load_3d(sA + a * kABytes, map, fb, k0, fa, it.e, pol_w);
+              tma_load_3d(sA + a * C::kABytes, map, fb, k0, fa, it.e, pol_w);
             } else if (a_atoms) {
               // 64 K rows x 128 features, features contiguous, as two 64-feature
               // atoms of a 4-D view: one box
-              tma_load_4d(sA + a * kABytes, map, fb, 0, k0, fa >> 6, it.e, pol_w);
+              tma_load_4d(sA + a * C::kABytes, map, fb, 0, k0, fa >> 6, it.e, pol_w);
             } else {
               // 64 K rows x 64 features per box: two boxes
-              tma_load_3d(sA + a * kABytes, map, fb, fa, k0, it.e, pol_w);
-              tma_load_3d(sA + a * kABytes + kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
+              tma_load_3d(sA + a * C::kABytes, map, fb, fa, k0, it.e, pol_w);
+              tma_load_3d(sA + a * C::kABytes + C::kAHalfBytes, map, fb, fa + 64, k0, it.e, pol_w);
             }
           }
           // the block's rows, rounded up to 32, in boxes of 256, 128, 64 and 32 rows
@@ -406,7 +547,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             const int lg = (kBN >= 256 && rem >= 256) ? 3 : (kBN >= 128 && rem >= 128) ? 2
                                                                 : rem >= 64             ? 1
                                                                                         : 0;
-            tma_load_2d(sB + r * 128, &bm[lg], fb, k0, it.row0 + r, pol_x);
+            tma_load_2d(sB + r * C::kRowBytes, &bm[lg], fb, k0, it.row0 + r, pol_x);
             r += kRowBox << lg;
           }
           ++issued;
@@ -466,7 +607,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           }
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
-          const uint32_t b0 = a0 + (uint32_t)(kNumA * kABytes);
+          const uint32_t b0 = a0 + (uint32_t)(kNumA * C::kABytes);
           if (C::kRegions > 0 && kb == kb0) {
             // First stage, one 64-token-column group at a time, each once the
             // epilogue has read it out of the previous tile.  Per accumulator
@@ -482,14 +623,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
               const int nr = n - c < 64 ? n - c : 64;
               const uint32_t idesc_r = idesc_bf16(BM, nr, /*a_mn=*/!kAKMajor, /*b_mn=*/false);
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk) {
+              for (int kk = 0; kk < kBK / 16; ++kk) {
                 // token row c starts c * 128 bytes into the K-major N operand
-                const uint64_t db = sdesc_sw128(b0 + c * 128 + kk * 32, 16, 1024);
+                const uint64_t db = sdesc_sw128(b0 + c * C::kRowBytes + kk * 32, 16, 1024);
 #pragma unroll
                 for (int a = 0; a < kNumA; ++a) {
                   const uint64_t da =
-                      kAKMajor ? sdesc_sw128(a0 + a * kABytes + kk * 32, 16, 1024)
-                               : sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024);
+                      kAKMajor ? sdesc_sw128(a0 + a * C::kABytes + kk * 32, 16, 1024)
+                               : sdesc_sw128(a0 + a * C::kABytes + kk * 2048, C::kAHalfBytes, 1024);
                   mma_bf16_ss(d0 + (uint32_t)(a * kBN + c), da, db, idesc_r, kk ? 1u : 0u);
                 }
               }
@@ -497,7 +638,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if (!ok) break;
           } else {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
+          for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accum = (kb > kb0 || kk) ? 1u : 0u;
             // N operand: K-major rows of 128 B; K step of 16 = 32 B inside the atom.
             const uint64_t db = sdesc_sw128(b0 + kk * 32, 16, 1024);
@@ -507,8 +648,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
               // per 1 KB group (SBO), K step of 16 = 16 rows = 2 KB.  K-major:
               // rows of 128 B, 8-row groups 1 KB apart, K step of 16 = 32 B.
               const uint64_t da =
-                  kAKMajor ? sdesc_sw128(a0 + a * kABytes + kk * 32, 16, 1024)
-                           : sdesc_sw128(a0 + a * kABytes + kk * 2048, kAHalfBytes, 1024);
+                  kAKMajor ? sdesc_sw128(a0 + a * C::kABytes + kk * 32, 16, 1024)
+                           : sdesc_sw128(a0 + a * C::kABytes + kk * 2048, C::kAHalfBytes, 1024);
               mma_bf16_ss(d0 + (uint32_t)(a * kBN), da, db, idesc, accum);
             }
           }
@@ -856,15 +997,23 @@ struct RowMap4 {
   CUtensorMap h[4];
 };
 
-template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false, bool kDualK = false>
+// Token rows gathered from x by the GEMM itself (see kGather).
+struct Gather {
+  const int32_t* sorted_src;   // row p of the expert groups is token sorted_src[p] / k
+  int k;
+};
+
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false, bool kDualK = false,
+          bool kGather = false>
 cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const RowMap4& b1,
                         const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
                         const OutMaps& outs, int* status, cudaStream_t s,
-                        StreamK sk = StreamK{nullptr, nullptr, 0, nullptr}) {
+                        StreamK sk = StreamK{nullptr, nullptr, 0, nullptr},
+                        Gather gather = Gather{nullptr, 1}) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
-  auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kGather>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -884,16 +1033,14 @@ cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const 
   }
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0.m, a1.m, rm, a0.atoms ? 1 : 0, offsets, block_off,
                                              num_blocks, block_expert, n_mt, K, out, ld_out,
-                                             M_total, aux, outs, sk, status);
+                                             M_total, aux, outs, sk, gather.sorted_src, gather.k,
+                                             status);
   return cudaGetLastError();
 }
 
-// FC2 pairs two W2 tiles when H allows it and K is long enough that the
-// single-buffered epilogue is a small share of a tile.
-#ifndef MOE_FC2_PAIR_MIN_F
-#define MOE_FC2_PAIR_MIN_F 0
-#endif
-bool fc2_paired(int H, int F) { return H % (2 * BM) == 0 && F >= MOE_FC2_PAIR_MIN_F; }
+// With 256-row blocks FC2 pairs two adjacent W2 tiles whenever H allows it
+// (measured faster than unpaired, double-buffered tiles on every large shape).
+bool fc2_paired(int H) { return H % (2 * BM) == 0; }
 
 struct PlanPtrs {
   const int32_t* offsets;
@@ -941,23 +1088,39 @@ bool map_rows(RowMap4* m, const void* X, int K, int P) {
   return true;
 }
 
+// x [T, K] (K contiguous) as the source of gathered token rows: boxes of one
+// row x 64 K (the only box height tile::gather4 takes), 128-byte swizzle.
+bool map_gather_rows(RowMap4* m, const void* X, int K, int T) {
+  const cuuint64_t d[2] = {(cuuint64_t)K, (cuuint64_t)T};
+  const cuuint64_t st[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, 1};
+  for (int j = 0; j < 4; ++j)
+    if (!make_map(&m->h[j], X, 2, d, st, box)) return false;
+  return true;
+}
+
 template <int kBN, int kBufs1>
 cudaError_t launch_fc1(const WMap& mW1, const WMap& mW3, const RowMap4& mX,
                        const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
-                       const EpiAux* save, int* status, cudaStream_t s, StreamK sk) {
+                       const EpiAux* save, int* status, cudaStream_t s, StreamK sk,
+                       const Gather* gather) {
   const long long nb_max = max_blocks(P, E, kBN);
   OutMaps om;
   if (!map_out(&om.m[0], h, F, P)) return cudaErrorInvalidValue;
+  if (gather != nullptr && save == nullptr)
+    return launch_gemm<2, kEpiSwiglu, kBN, kBufs1, false, false, true>(
+        mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max,
+        h, F, EpiAux{}, om, status, s, sk, *gather);
   if (save != nullptr) {
     if (!map_out(&om.m[1], save->g, save->ld, P) || !map_out(&om.m[2], save->u, save->ld, P))
       return cudaErrorInvalidValue;
-    return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
-                                                       pl.num_blocks, pl.block_expert, F, H,
-                                                       nb_max, h, F, *save, om, status, s, sk);
+    return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(
+        mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max,
+        h, F, *save, om, status, s, sk);
   }
-  return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(mW1, mW3, mX, mX, pl.offsets, pl.block_off,
-                                                 pl.num_blocks, pl.block_expert, F, H, nb_max, h,
-                                                 F, EpiAux{}, om, status, s, sk);
+  return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(
+      mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max, h,
+      F, EpiAux{}, om, status, s, sk);
 }
 
 template <int kNumA, int kBN, int kBufs>
@@ -966,10 +1129,9 @@ cudaError_t launch_fc2(const WMap& mW2, const RowMap4& mH, const PlanPtrs& pl, i
                        StreamK sk = StreamK{nullptr, nullptr, 0, nullptr}) {
   OutMaps om;
   if (!map_out(&om.m[0], y, H, P)) return cudaErrorInvalidValue;
-  return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(mW2, mW2, mH, mH, pl.offsets, pl.block_off,
-                                                  pl.num_blocks, pl.block_expert, H, F,
-                                                  max_blocks(P, E, kBN), y, H, EpiAux{}, om,
-                                                  status, s, sk);
+  return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(
+      mW2, mW2, mH, mH, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
+      max_blocks(P, E, kBN), y, H, EpiAux{}, om, status, s, sk);
 }
 
 // kPairF / kPairH: pair adjacent weight tiles (single-buffered accumulators)
@@ -1018,16 +1180,21 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
                                cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save,
-                               const StreamKSpace* sks) {
+                               const StreamKSpace* sks, const GatherRows* gather_rows) {
   if (P == 0) return cudaSuccess;
+  const bool gathered = gather_rows != nullptr && save == nullptr;
+  const FfnMode mode = ffn_mode(P, E);
   WMap mW1, mW3, mW2;
   RowMap4 mX, mH;
   if (!map_weights_mn(&mW1, W1, H, F, E) || !map_weights_mn(&mW3, W3, H, F, E) ||
-      !map_weights_mn(&mW2, W2, F, H, E) || !map_rows(&mX, x_perm, H, P) ||
-      !map_rows(&mH, h, F, P))
+      !map_weights_mn(&mW2, W2, F, H, E) || !map_rows(&mH, h, F, P))
     return cudaErrorInvalidValue;
+  if (gathered ? !map_gather_rows(&mX, gather_rows->x, H, gather_rows->T)
+               : !map_rows(&mX, x_perm, H, P))
+    return cudaErrorInvalidValue;
+  const Gather g{gathered ? gather_rows->sorted_src : nullptr, gathered ? gather_rows->k : 1};
+  const Gather* gp = gathered ? &g : nullptr;
   const PlanPtrs pl{offsets, block_off, num_blocks, block_expert};
-  const FfnMode mode = ffn_mode(P, E);
   // Balanced K split when the tiles do not fill the SMs evenly.  Tiles come
   // from the on-device queue when their costs differ: 256-row blocks with
   // fewer than two blocks per expert on average, where one expert's rows fill
@@ -1041,18 +1208,19 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
           : StreamK{nullptr, nullptr, 0, nullptr};
   cudaError_t err;
   if (mode == FfnMode::kTiny)
-    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
+    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp);
   else if (mode == FfnMode::kSmall)
-    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
+    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp);
   else
-    err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk);
+    err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk,
+                                         gp);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
   if (mode == FfnMode::kTiny)
     return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   if (mode == FfnMode::kSmall)
     return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
-  if (fc2_paired(H, F))
+  if (fc2_paired(H))
     return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
   return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
 }

@@ -99,7 +99,8 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                           const void* W2, int T, int H, int F, int E, int k, void* out,
                           void* ws, const WsLayout& L, cudaStream_t s,
                           const cudaEvent_t* ev = nullptr, bool clear = true,
-                          const SharedExpert* sh = nullptr, const EpiAux* save = nullptr) {
+                          const SharedExpert* sh = nullptr, const EpiAux* save = nullptr,
+                          bool out_f32 = false) {
   const int P = T * k;
   const int C = num_chunks(T, k);
   int* status = ws_ptr<int>(ws, L.status);
@@ -134,17 +135,23 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
   MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
                       ffn_block_rows(P, E, H, F), s, pdl));
   MOE_TRY(mark(2));
-  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s, pdl));
+  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, offsets, sorted_src, dest_of, s, pdl));
   MOE_TRY(mark(3));
-  MOE_TRY(launch_gather_tokens(static_cast<const __nv_bfloat16*>(x), dest_of, T, H, k, x_perm, s,
-                               pdl));
+  // With small token blocks FC1 gathers its rows from x itself; otherwise (and
+  // in the forward with saves, whose rows the backward's WGrad reads) they are
+  // first copied into expert order (x_perm), each row of x read once.
+  const bool gathers = save == nullptr && ffn_gathers_rows(P, E);
+  if (!gathers)
+    MOE_TRY(launch_gather_tokens(static_cast<const __nv_bfloat16*>(x), dest_of, T, H, k, x_perm,
+                                 s, pdl));
   MOE_TRY(mark(4));
+  const GatherRows gr{static_cast<const __nv_bfloat16*>(x), sorted_src, k, T};
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
-                             ev ? ev[5] : nullptr, save, &sks));
+                             ev ? ev[5] : nullptr, save, &sks, gathers ? &gr : nullptr));
   if (sh != nullptr)
     MOE_TRY(launch_grouped_ffn(static_cast<const __nv_bfloat16*>(x), sh->plan.offsets,
                                sh->plan.block_off, sh->plan.num_blocks, sh->plan.block_expert,
@@ -153,8 +160,11 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                                static_cast<const __nv_bfloat16*>(sh->W2), T, H, sh->Fs, 1, sh->h,
                                sh->y, status, s));   // its block size differs: no split
   MOE_TRY(mark(6));
-  MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
-                         sh ? sh->y : nullptr, pdl));
+  if (out_f32)
+    MOE_TRY(launch_combine_f32(y, dest_of, topk_w, T, H, k, static_cast<float*>(out), s, pdl));
+  else
+    MOE_TRY(launch_combine(y, dest_of, topk_w, T, H, k, static_cast<__nv_bfloat16*>(out), s,
+                           sh ? sh->y : nullptr, pdl));
   MOE_TRY(mark(7));
   return MOE_OK;
 }
@@ -208,7 +218,7 @@ moe_status moe_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* co
   MOE_TRY(launch_scan(chunk, C, E, counts, offsets, ws_ptr<int32_t>(ws, L.block_off),
                       ws_ptr<int32_t>(ws, L.num_blocks), ws_ptr<int32_t>(ws, L.block_expert),
                       kBlockRows, s));
-  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s));
+  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, offsets, sorted_src, dest_of, s));
   return MOE_OK;
 }
 
@@ -230,20 +240,25 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   int32_t* block_off = ws_ptr<int32_t>(ws, L.block_off);
   int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
   int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
-  __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
   // the status word and FC2's split counters (adjacent) start at zero
   MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kSkCntInts * sizeof(int), s));
-  MOE_TRY(launch_plan(offsets, E, block_off, num_blocks, block_expert,
-                      ffn_block_rows(P, E, H, F), s));
-  MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
+  MOE_TRY(launch_plan(offsets, E, P, block_off, num_blocks, block_expert,
+                      ffn_block_rows(P, E, H, F), status, s));
+  // with small token blocks FC1 gathers the rows of x itself (row p = token
+  // sorted_src[p] / k); otherwise they are copied into expert order first
+  const bool gathers = ffn_gathers_rows(P, E);
+  __nv_bfloat16* x_perm = ws_ptr<__nv_bfloat16>(ws, L.x_perm);
+  if (!gathers)
+    MOE_TRY(launch_gather(static_cast<const __nv_bfloat16*>(x), sorted_src, P, H, k, x_perm, s));
+  const GatherRows gr{static_cast<const __nv_bfloat16*>(x), sorted_src, k, T};
   MOE_TRY(launch_grouped_ffn(x_perm, offsets, block_off, num_blocks, block_expert,
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E,
                              ws_ptr<__nv_bfloat16>(ws, L.h),
                              static_cast<__nv_bfloat16*>(y_sorted), status, s, nullptr, nullptr,
-                             &sks));
+                             &sks, gathers ? &gr : nullptr));
   return MOE_OK;
 }
 
@@ -274,6 +289,30 @@ moe_status moe_forward(const void* x, const float* router_logits, const void* W1
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L,
                         static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_f32(const void* x, const float* router_logits, const void* W1,
+                           const void* W3, const void* W2, int T, int H, int F, int E, int k,
+                           float* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L,
+                        static_cast<cudaStream_t>(stream), nullptr, true, nullptr, nullptr,
+                        /*out_f32=*/true);
+}
+
+moe_status moe_cast_bf16(const float* in, void* out, size_t n, void* stream) {
+  if (n == 0) return MOE_OK;
+  if (!ok_ptr(in) || !ok_ptr(out) || n >= ((size_t)1 << 40)) return MOE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_cast_bf16(in, static_cast<__nv_bfloat16*>(out), n,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_forward_events(const void* x, const float* router_logits, const void* W1,
@@ -316,10 +355,6 @@ void* mapped_host(const void* p) {
 }
 }  // namespace
 
-#ifndef MOE_HOST_X_IN_PLACE_MAX
-#define MOE_HOST_X_IN_PLACE_MAX (1ull << 62)
-#endif
-
 moe_status moe_forward_host(const void* x_host, const float* logits_host, const void* W1,
                             const void* W3, const void* W2, int T, int H, int F, int E, int k,
                             void* out_host, void* ws, size_t ws_bytes, void* stream) {
@@ -334,10 +369,10 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // A page-locked, mapped host buffer is used in place: the kernels load x
   // and the logits and store the result over the host link, each element
-  // once, with no staging copy (x up to MOE_HOST_X_IN_PLACE_MAX bytes).  Any
-  // other host buffer goes through a staging region of ws.
-  const bool small = (size_t)T * H * 2 <= (size_t)MOE_HOST_X_IN_PLACE_MAX;
-  void* xm = small ? mapped_host(x_host) : nullptr;
+  // once, with no staging copy.  Any other host buffer goes through a staging
+  // region of ws, and so does x when FC1 gathers its rows from x itself (it
+  // would read each row once per feature tile).
+  void* xm = ffn_gathers_rows((long long)T * k, E) ? nullptr : mapped_host(x_host);
   void* lm = mapped_host(logits_host);
   void* om = mapped_host(out_host);   // the combine writes each result row once
   void* dx = xm ? xm : ws_ptr<void>(ws, L.stage_x);
@@ -496,6 +531,29 @@ moe_status moe_backward(const void* dout, const float* router_logits, const void
                        static_cast<__nv_bfloat16*>(dW1), static_cast<__nv_bfloat16*>(dW3),
                        static_cast<__nv_bfloat16*>(dW2), status, s));
   return MOE_OK;
+}
+
+size_t moe_plan_workspace_size(int E, int G) {
+  if (E < 1 || E > MOE_MAX_EXPERTS || G < 1 || G > MOE_PLAN_MAX_GPUS || G > E) return 0;
+  return plan_ws_bytes(E, G);
+}
+
+moe_status moe_plan_replicas(const int32_t* counts, int E, int G, int beta, int budget,
+                             int rounds, int lambda, int32_t* blocks_per_gpu,
+                             int32_t* row_ranges, int32_t* gpu_load, int32_t* info, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (E < 1 || E > MOE_MAX_EXPERTS || G < 1 || G > MOE_PLAN_MAX_GPUS || G > E || beta < 1 ||
+      budget < 0 || budget > E || rounds < -1 || rounds > 1 << 20 || lambda < -1)
+    return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(counts) || !ok_ptr(blocks_per_gpu) || !ok_ptr(row_ranges) || !ok_ptr(gpu_load) ||
+      !ok_ptr(info))
+    return MOE_ERR_INVALID_ARG;
+  if (check_ws(ws, ws_bytes, plan_ws_bytes(E, G)) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  const int s_rounds = rounds < 0 ? budget : rounds;
+  return cuda_status(launch_plan_replicas(counts, E, G, beta, budget, s_rounds + 2, lambda, ws,
+                                          blocks_per_gpu, row_ranges, gpu_load, info,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_get_device_status(const void* ws, void* stream) {

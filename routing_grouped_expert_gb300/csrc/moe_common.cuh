@@ -132,7 +132,7 @@ struct GatedLayout {
   size_t total;
 };
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline __host__ __device__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   const size_t P = (size_t)T * k;
@@ -239,14 +239,27 @@ cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* 
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
                         int beta, cudaStream_t s, bool pdl = false);
+// Out-of-range expert indices take no position: dest_of = -1 for them and
+// sorted_src[offsets[E] .. T*k) = -1.
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
-                           const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
-                           cudaStream_t s, bool pdl = false);
-cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
-                        int32_t* block_expert, int beta, cudaStream_t s);
+                           const int32_t* chunk_base, const int32_t* offsets,
+                           int32_t* sorted_src, int32_t* dest_of, cudaStream_t s,
+                           bool pdl = false);
+// Block plan of caller-supplied offsets of P rows; offsets that do not group
+// P rows set MOE_ERR_INVALID_ARG in `status` and leave an empty plan.
+cudaError_t launch_plan(const int32_t* offsets, int E, int P, int32_t* block_off,
+                        int32_t* num_blocks, int32_t* block_expert, int beta, int* status,
+                        cudaStream_t s);
 // Token-block rows (beta) the grouped FFN uses for a layer of these sizes;
 // the block plan must be built with the same value.
 int ffn_block_rows(int P, int E, int H, int F);
+// True when FC1 gathers its token rows from x itself (tile::gather4 loads,
+// four rows per instruction) instead of reading an expert-ordered copy
+// x_perm: only with small token blocks (the tiny mode, at most 64 rows), where
+// a stage's gather instructions take less time than its MMAs.  Measured: with
+// 256-row blocks the gather loads made the fine-grained FC1 2.6x slower.
+inline bool ffn_gathers_rows(long long P, int E) { return ffn_mode(P, E) == FfnMode::kTiny; }
+// x_perm[p] = x[sorted_src[p] / k] (positions holding -1 skipped).
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,
                           __nv_bfloat16* x_perm, cudaStream_t s, bool pdl = false);
 // The same rows from the token side: x_perm[dest_of[t * k + j]] = x[t], each
@@ -270,8 +283,17 @@ struct StreamKSpace {
   int* cnt;            // [kSkCntInts]: split counters, then the queue head at kStreamKMaxCtas
   size_t slot_bytes;
 };
-// FC1 (+SwiGLU) and FC2 over the expert groups.  With `save`, FC1 also keeps
-// its pre-activations g = x W1, u = x W3 (bf16, [P, F]) for the backward.
+// Where FC1 takes its token rows from when it gathers them itself: row p of
+// the expert groups is x[sorted_src[p] / k].
+struct GatherRows {
+  const __nv_bfloat16* x;      // [T, H]
+  const int32_t* sorted_src;   // [T * k]
+  int k, T;
+};
+// FC1 (+SwiGLU) and FC2 over the expert groups.  FC1's token rows are rows of
+// x_perm (expert order), or, with `gather` (and no `save`), gathered from x
+// by the GEMM's own loads.  With `save`, FC1 also keeps its pre-activations
+// g = x W1, u = x W3 (bf16, [P, F]) for the backward.
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                const int32_t* block_off, const int32_t* num_blocks,
                                const int32_t* block_expert, const __nv_bfloat16* W1,
@@ -279,7 +301,8 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
                                cudaStream_t s, cudaEvent_t after_fc1 = nullptr,
                                const EpiAux* save = nullptr,
-                               const StreamKSpace* sks = nullptr);
+                               const StreamKSpace* sks = nullptr,
+                               const GatherRows* gather = nullptr);
 // Backward DGrad of both expert GEMMs: dh = dY W2^T -> dg, du (SwiGLU
 // derivative from the saved g, u), dx_perm = dg W1^T + du W3^T.
 cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,
@@ -294,6 +317,14 @@ cudaError_t launch_combine(const __nv_bfloat16* y_sorted, const int32_t* dest_of
                            const float* topk_w, int T, int H, int k, __nv_bfloat16* out,
                            cudaStream_t s, const __nv_bfloat16* y_shared = nullptr,
                            bool pdl = false);
+
+// The same sum left in fp32 (no rounding), no shared expert.
+cudaError_t launch_combine_f32(const __nv_bfloat16* y_sorted, const int32_t* dest_of,
+                               const float* topk_w, int T, int H, int k, float* out,
+                               cudaStream_t s, bool pdl = false);
+
+// out[i] = bf16(in[i]) (round to nearest even).
+cudaError_t launch_cast_bf16(const float* in, __nv_bfloat16* out, size_t n, cudaStream_t s);
 
 // Block plan of one expert that takes every token in order (router GEMM,
 // shared expert): offsets = {0, T}.
@@ -328,6 +359,14 @@ cudaError_t launch_wgrad(const __nv_bfloat16* x_perm, const __nv_bfloat16* h,
                          const __nv_bfloat16* du, const int32_t* offsets, int P, int H, int F,
                          int E, __nv_bfloat16* dW1, __nv_bfloat16* dW3, __nv_bfloat16* dW2,
                          int* status, cudaStream_t s);
+
+// The expert-replica planner (planner.cu): workspace bytes and launch.
+// rounds = the searches' round limit (s + 2); lam < 0: no reduction penalty.
+size_t plan_ws_bytes(int E, int G);
+cudaError_t launch_plan_replicas(const int32_t* counts, int E, int G, int beta, int budget,
+                                 int rounds, long long lam, void* ws, int32_t* n_out,
+                                 int32_t* rows_out, int32_t* load_out, int32_t* info,
+                                 cudaStream_t s);
 
 // bf16 TMA tensor map with a 128-byte swizzle; dims/strides innermost first.
 bool make_tensor_map_bf16(void* map /* CUtensorMap* */, const void* base, int rank,

@@ -106,19 +106,40 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict_
   write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
 }
 
+// The block plan of caller-supplied offsets (moe_grouped_ffn).  Offsets that
+// are not a valid grouping of P rows (offsets[0] != 0, a decrease, or
+// offsets[E] > P) would size the plan past its table: they set
+// MOE_ERR_INVALID_ARG and leave an empty plan, so the GEMMs do nothing.
 __global__ void __launch_bounds__(kScanThreads)
-plan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ block_off,
-            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta) {
+plan_kernel(const int32_t* __restrict__ offsets, int E, int P, int32_t* __restrict__ block_off,
+            int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta,
+            int* __restrict__ status) {
   __shared__ int warp_sums[33];
+  __shared__ int bad;
   const int e = threadIdx.x;
+  if (e == 0) bad = offsets[0] != 0 || offsets[E] > P;
+  __syncthreads();
   const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
+  if (cnt < 0) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (e == 0) {
+      if (status != nullptr) set_status(status, MOE_ERR_INVALID_ARG);
+      block_off[E] = 0;
+      *num_blocks = 0;
+    }
+    return;
+  }
   write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
 }
 
+// An assignment whose expert index is out of range takes no position:
+// dest_of[a] = -1, and the positions past the valid ones, [offsets[E], P),
+// hold -1 in sorted_src (the gather and the combine skip both).
 __global__ void __launch_bounds__(kChunkAssign)
 scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_assign,
-               const int32_t* __restrict__ chunk_base, int32_t* __restrict__ sorted_src,
-               int32_t* __restrict__ dest_of) {
+               const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+               int32_t* __restrict__ sorted_src, int32_t* __restrict__ dest_of) {
   extern __shared__ int cnt[];   // [warps][E]
   pdl_wait();
   pdl_trigger();
@@ -146,12 +167,16 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_ass
     const int pos = chunk_base[(size_t)blockIdx.x * E + e] + cnt[warp * E + e] + rank_w;
     sorted_src[pos] = a;
     dest_of[a] = pos;
+  } else if (threadIdx.x < chunk_assign && a < P) {
+    dest_of[a] = -1;
   }
+  // the valid assignments fill [0, offsets[E]); mark the rest of sorted_src
+  if (threadIdx.x < chunk_assign && a < P && a >= offsets[E]) sorted_src[a] = -1;
 }
 
 // x_perm[p] = x[sorted_src[p] / k]: one warp per segment of 4 x 32 16-byte
 // vectors of a row (segments grid-strided), all four loads of a lane in
-// flight before its stores.
+// flight before its stores.  Positions holding -1 (no assignment) are skipped.
 constexpr int kGatherUnroll = 4;
 __global__ void __launch_bounds__(256)
 gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sorted_src, int P,
@@ -167,17 +192,17 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ s
        w += (long long)gridDim.x * wpb) {
     const int row = (int)(w / upr);
     const int v0 = (int)(w - (long long)row * upr) * 32 * kGatherUnroll + lane;
-    const int4* src = reinterpret_cast<const int4*>(x) + (size_t)(__ldg(sorted_src + row) / k) * nv;
+    const int a = __ldg(sorted_src + row);
+    if (a < 0 || a >= P) continue;   // no assignment at this position
+    const int4* src = reinterpret_cast<const int4*>(x) + (size_t)(a / k) * nv;
     int4* dst = reinterpret_cast<int4*>(x_perm) + (size_t)row * nv;
-    {
-      int4 r[kGatherUnroll];
+    int4 r[kGatherUnroll];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u)
-        if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
+    for (int u = 0; u < kGatherUnroll; ++u)
+      if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u)
-        if (v0 + 32 * u < nv) dst[v0 + 32 * u] = r[u];
-    }
+    for (int u = 0; u < kGatherUnroll; ++u)
+      if (v0 + 32 * u < nv) dst[v0 + 32 * u] = r[u];
   }
 }
 
@@ -205,7 +230,9 @@ gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restr
     for (int u = 0; u < kGatherUnroll; ++u)
       if (v0 + 32 * u < nv) r[u] = __ldg(src + v0 + 32 * u);
     for (int j = 0; j < k; ++j) {
-      int4* dst = reinterpret_cast<int4*>(x_perm) + (size_t)__ldg(dest_of + (size_t)t * k + j) * nv;
+      const int p = __ldg(dest_of + (size_t)t * k + j);
+      if (p < 0) continue;   // an assignment that took no position
+      int4* dst = reinterpret_cast<int4*>(x_perm) + (size_t)p * nv;
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u)
         if (v0 + 32 * u < nv) dst[v0 + 32 * u] = r[u];
@@ -222,15 +249,17 @@ cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int3
                   offsets, block_off, num_blocks, block_expert, beta);
 }
 
-cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* block_off, int32_t* num_blocks,
-                        int32_t* block_expert, int beta, cudaStream_t s) {
-  plan_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, block_off, num_blocks, block_expert, beta);
+cudaError_t launch_plan(const int32_t* offsets, int E, int P, int32_t* block_off,
+                        int32_t* num_blocks, int32_t* block_expert, int beta, int* status,
+                        cudaStream_t s) {
+  plan_kernel<<<1, kScanThreads, 0, s>>>(offsets, E, P, block_off, num_blocks, block_expert, beta,
+                                         status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
-                           const int32_t* chunk_base, int32_t* sorted_src, int32_t* dest_of,
-                           cudaStream_t s, bool pdl) {
+                           const int32_t* chunk_base, const int32_t* offsets,
+                           int32_t* sorted_src, int32_t* dest_of, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int C = num_chunks(T, k);
   const int chunk_assign = tokens_per_chunk(k) * k;
@@ -241,7 +270,7 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
       (int)((kChunkAssign / 32) * MOE_MAX_EXPERTS * sizeof(int)));
   if (err != cudaSuccess) return err;
   return launch_k(scatter_kernel, dim3(C), dim3(kChunkAssign), smem, s, pdl, topk_idx, T * k, E,
-                  chunk_assign, chunk_base, sorted_src, dest_of);
+                  chunk_assign, chunk_base, offsets, sorted_src, dest_of);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted_src, int P, int H, int k,

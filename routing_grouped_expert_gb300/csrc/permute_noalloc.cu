@@ -3,7 +3,9 @@
 // block plan and a status word -- lives in one fixed array in device memory
 // instead of a caller-supplied workspace.  The kernels are the same ones
 // moe_permute launches; only where their scratch lives differs.
-#include <atomic>
+#include <cuda.h>
+
+#include <mutex>
 
 #include "moe_common.cuh"
 
@@ -16,10 +18,6 @@ static __device__ __align__(256) int32_t g_permute_scratch[MOE_PERMUTE_NOALLOC_S
 namespace {
 
 constexpr size_t kScratchInts = MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / sizeof(int32_t);
-constexpr int kMaxDevices = 64;
-// Device address of g_permute_scratch, looked up once per device.  In host
-// code the array's name is only a host-side stand-in, never a device pointer.
-std::atomic<int32_t*> g_scratch_addr[kMaxDevices];
 
 size_t round64(size_t v) { return (v + 63) / 64 * 64; }
 
@@ -30,20 +28,64 @@ size_t scratch_ints(int T, int E, int k) {
   return 64 + round64(C * E) + round64((size_t)E + 1) + 64 + round64(NB);
 }
 
+// The device address of g_permute_scratch differs per CUDA context (each
+// context loads the library's device code on its own, and a device reset
+// replaces the context), so it is looked up once per context, keyed by the
+// context's process-unique ID.  In host code the array's name is only a
+// host-side stand-in, never a device pointer.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+struct AddrCache {
+  std::mutex mu;
+  static constexpr int kSlots = 64;
+  unsigned long long ctx_id[kSlots] = {};
+  int32_t* addr[kSlots] = {};
+  int next = 0;
+};
+AddrCache g_cache;
+
 cudaError_t scratch_address(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int32_t* a = g_scratch_addr[dev].load(std::memory_order_relaxed);
-  if (a == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (get_ctx == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {
+    // no context yet on this thread: cudaSetDevice makes the current device's
+    // primary context current (creating it if needed)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
     if (e != cudaSuccess) return e;
-    a = static_cast<int32_t*>(p);
-    g_scratch_addr[dev].store(a, std::memory_order_relaxed);
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
   }
-  *out = a;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  std::lock_guard<std::mutex> lock(g_cache.mu);
+  for (int i = 0; i < AddrCache::kSlots; ++i)
+    if (g_cache.addr[i] != nullptr && g_cache.ctx_id[i] == id) {
+      *out = g_cache.addr[i];
+      return cudaSuccess;
+    }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  if (e != cudaSuccess) return e;
+  const int slot = g_cache.next;
+  g_cache.next = (slot + 1) % AddrCache::kSlots;
+  g_cache.ctx_id[slot] = id;
+  g_cache.addr[slot] = static_cast<int32_t*>(p);
+  *out = g_cache.addr[slot];
   return cudaSuccess;
 }
 
@@ -89,7 +131,8 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_idx, int T, int E,
       moe::launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
                        moe::kBlockRows, s) !=
           cudaSuccess ||
-      moe::launch_scatter(topk_idx, T, E, k, chunk, sorted_src, dest_of, s) != cudaSuccess)
+      moe::launch_scatter(topk_idx, T, E, k, chunk, offsets, sorted_src, dest_of, s) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

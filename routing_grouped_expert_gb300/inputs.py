@@ -21,7 +21,8 @@ Recipe (every workload):
   W2 (down)      bf16 [E, F, H] ~ N(0, 1/F), seed 4;
   expert ranking for the skew bias: a random permutation, seed 5.
 Weights are drawn one expert at a time in fp32 and rounded to bf16, so the
-transient fp32 buffer is one expert's matrix.
+transient fp32 buffer is one expert's matrix.  Further realizations of a
+workload (the benchmark's median over several) shift every seed by 1000 r.
 """
 from __future__ import annotations
 
@@ -42,6 +43,7 @@ class Workload:
     skew_alpha: float = 0.0   # 0 = uniform routing
     zipf_s: float = 1.2
     note: str = ""
+    realization: int = 0      # r > 0: every seed below shifted by 1000 r
 
     def with_(self, **kw) -> "Workload":
         d = dict(self.__dict__)
@@ -85,12 +87,17 @@ def zipf_bias(E: int, alpha: float, s: float = 1.2, seed: int = SEED_PERM) -> to
     return alpha * torch.log(w[perm])
 
 
+def _seed(wl: Workload, base: int) -> int:
+    return base + 1000 * wl.realization
+
+
 def make_logits(wl: Workload) -> torch.Tensor:
     """fp32 [T, E] router logits, always drawn on the CPU."""
-    g = torch.Generator().manual_seed(SEED_LOGITS)
+    g = torch.Generator().manual_seed(_seed(wl, SEED_LOGITS))
     logits = torch.randn(wl.T, wl.E, generator=g, dtype=torch.float32)
     if wl.skew_alpha != 0.0:
-        logits = logits + zipf_bias(wl.E, wl.skew_alpha, wl.zipf_s).to(torch.float32)
+        logits = logits + zipf_bias(wl.E, wl.skew_alpha, wl.zipf_s,
+                                    seed=_seed(wl, SEED_PERM)).to(torch.float32)
     return logits
 
 
@@ -102,7 +109,7 @@ def _randn_bf16(shape, std: float, gen: torch.Generator, device) -> torch.Tensor
 
 
 def make_x(wl: Workload, device="cpu") -> torch.Tensor:
-    g = torch.Generator(device=device).manual_seed(SEED_X)
+    g = torch.Generator(device=device).manual_seed(_seed(wl, SEED_X))
     return _randn_bf16((wl.T, wl.H), 1.0, g, device)
 
 
@@ -112,7 +119,7 @@ def make_weights(wl: Workload, device="cpu"):
     for seed, (r, c), std in ((SEED_W1, (wl.H, wl.F), 1.0 / math.sqrt(wl.H)),
                               (SEED_W3, (wl.H, wl.F), 1.0 / math.sqrt(wl.H)),
                               (SEED_W2, (wl.F, wl.H), 1.0 / math.sqrt(wl.F))):
-        g = torch.Generator(device=device).manual_seed(seed)
+        g = torch.Generator(device=device).manual_seed(_seed(wl, seed))
         W = torch.empty(wl.E, r, c, dtype=torch.bfloat16, device=device)
         for e in range(wl.E):
             W[e] = _randn_bf16((r, c), std, g, device)

@@ -18,7 +18,32 @@ CASES = {  # name: (T, H, F, E, k, slices)
     "decode_like_2": (64, 512, 1024, 8, 2, 2),
     "large_blocks_4": (600, 256, 512, 2, 2, 4),
     "many_experts_2": (300, 256, 256, 32, 4, 2),
+    "fine_grained_like_2": (512, 512, 512, 16, 8, 2),
 }
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fp32_partials_sum_to_the_layer(name):
+    """The feature-sharded runner's arithmetic on one GPU: moe_forward_f32 on
+    each slice (unrounded fp32 partials), summed in fp32 as the all-reduce
+    would, rounded to bf16 once by moe_cast_bf16."""
+    from routing_grouped_expert_gb300 import sharded
+    T, H, F, E, k, G = CASES[name]
+    wl = I.small(name, T=T, H=H, F=F, E=E, k=k)
+    d = I.make_inputs(wl, "cpu")
+    dev = {n: t.cuda() for n, t in d.items()}
+    acc = torch.zeros(T, H, dtype=torch.float32, device="cuda")
+    for r in range(G):
+        W1s, W3s, W2s = sharded.shard_weights(dev["W1"], dev["W3"], dev["W2"], G, r)
+        acc += moe.moe_forward_f32(dev["x"], dev["logits"], W1s, W3s, W2s, k)
+    out = moe.moe_cast_bf16(acc)
+    ref = O.forward_perm(d["x"], d["logits"].numpy(), d["W1"], d["W3"], d["W2"], k)["out"]
+    assert_moe_close(out, ref, f"{name}: fp32 partials of {G} feature slices")
+    # the unsharded fp32 output rounds to the plain layer's bits
+    whole = moe.moe_forward_f32(dev["x"], dev["logits"], dev["W1"], dev["W3"], dev["W2"], k)
+    plain = moe.moe_forward(dev["x"], dev["logits"], dev["W1"], dev["W3"], dev["W2"], k)
+    assert torch.equal(moe.moe_cast_bf16(whole), plain)
+    assert torch.equal(whole.to(torch.bfloat16), plain)
 
 
 @pytest.mark.parametrize("name", list(CASES))

@@ -59,3 +59,37 @@ def test_full_size_host_buffers(name):
     out_h = moe.moe_forward_host(xh, lh, d["W1"], d["W3"], d["W2"], wl.k)
     torch.cuda.current_stream().synchronize()
     assert torch.equal(out_h, out.cpu())
+
+
+def chosen_experts(counts, E, beta_rows):
+    """Experts whose every row is compared: the hottest, one cut into several
+    token blocks, the last expert (its tiles end the tile list, where the
+    balanced K split cuts them), the coldest non-empty one and the first."""
+    nz = np.nonzero(counts)[0]
+    pick = [int(np.argmax(counts)), int(nz[-1]), int(nz[np.argmin(counts[nz])]), int(nz[0])]
+    multi = np.nonzero(counts > beta_rows)[0]
+    if multi.size:
+        pick.append(int(multi[len(multi) // 2]))
+    return list(dict.fromkeys(pick))
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_whole_experts(name):
+    """Every row of a few chosen experts at full size: the grouped FFN run on the
+    full batch's permutation (the same GEMM launches as the layer's) against the
+    oracle's FFN of those experts, element by element."""
+    wl = I.WORKLOADS[name]
+    d = I.make_inputs(wl, "cuda")
+    idx, _ = moe.moe_route_topk(d["logits"], wl.k)
+    counts, offsets, sorted_src, _ = moe.moe_permute(idx, wl.E)
+    y = moe.moe_grouped_ffn(d["x"], sorted_src, offsets, d["W1"], d["W3"], d["W2"], wl.k)
+    torch.cuda.synchronize()
+    c, off, src = to_np(counts), to_np(offsets), to_np(sorted_src)
+    mean = wl.T * wl.k / wl.E
+    beta = 64 if mean <= 40 else 128 if mean <= 80 else 256
+    x_cpu = d["x"].cpu()
+    for e in chosen_experts(c, wl.E, beta):
+        lo, hi = int(off[e]), int(off[e + 1])
+        ref = O.expert_ffn(x_cpu[torch.from_numpy(src[lo:hi] // wl.k)], d["W1"][e].cpu(),
+                           d["W3"][e].cpu(), d["W2"][e].cpu())
+        assert_moe_close(y[lo:hi], ref, f"{name} expert {e} ({hi - lo} rows)")

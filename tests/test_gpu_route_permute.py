@@ -74,13 +74,56 @@ def test_nonfinite_logit_reported_and_indices_stay_in_range():
     assert moe.moe_get_device_status(ws) == 0
 
 
-def test_out_of_range_expert_index_reported():
-    idx = torch.randint(0, 8, (64, 2), dtype=torch.int32)
+def expected_with_bad_indices(idx, E):
+    """What the permute must give when some expert indices are out of range:
+    the valid assignments grouped exactly as the oracle groups them (the bad
+    ones relabelled as an extra expert E, which sorts them last), and -1 for
+    the bad ones' dest_of and for the tail of sorted_src."""
+    flat = idx.reshape(-1).copy()
+    bad = (flat < 0) | (flat >= E)
+    flat[bad] = E
+    counts, offsets, src, dest = O.permute(flat.reshape(idx.shape), E + 1)
+    src = src.copy()
+    dest = dest.copy()
+    src[offsets[E]:] = -1
+    dest[bad] = -1
+    return counts[:E], offsets[:E + 1], src, dest
+
+
+def test_out_of_range_expert_index_reported_and_marked():
+    idx = torch.randint(0, 8, (700, 2), dtype=torch.int32, generator=torch.Generator().manual_seed(9))
     idx[10, 1] = 8
     idx[20, 0] = -1
+    idx[650, 1] = 1 << 30
     ws = moe.Workspace()
-    moe.moe_permute(idx.cuda(), 8, ws=ws)
+    # outputs pre-filled with garbage: the marks must be written, not left over
+    out = tuple(torch.full((n,), 12345, dtype=torch.int32, device="cuda")
+                for n in (8, 9, 1400, 1400))
+    counts, off, src, dest = moe.moe_permute(idx.cuda(), 8, ws=ws, out=out)
     assert moe.moe_get_device_status(ws) == 1   # MOE_ERR_INVALID_ARG
+    want = expected_with_bad_indices(idx.numpy(), 8)
+    for name, got, w in zip(("counts", "offsets", "sorted_src", "dest_of"),
+                            (counts, off, src, dest), want):
+        np.testing.assert_array_equal(to_np(got), w, err_msg=name)
+
+
+def test_combine_skips_assignments_that_took_no_position():
+    """A slot with dest_of = -1 adds nothing: out[t] sums its valid slots."""
+    T, H, k = 50, 256, 3
+    g = torch.Generator().manual_seed(3)
+    y = torch.randn(T * k, H, generator=g).to(torch.bfloat16)
+    dest = torch.randperm(T * k, generator=g).to(torch.int32)
+    w = torch.rand(T, k, generator=g)
+    dest[7] = -1
+    dest[100] = -1
+    out = moe.moe_combine(y.cuda(), dest.cuda(), w.cuda())
+    d = dest.numpy().reshape(T, k)
+    ref = np.zeros((T, H))
+    for j in range(k):        # slot order, the oracle's combine on the valid slots
+        ok = d[:, j] >= 0
+        ref[ok] += w.numpy()[ok, j:j + 1].astype(np.float64) * \
+            y.double().numpy()[d[ok, j]]
+    np.testing.assert_allclose(to_np(out.double()), ref, rtol=2 ** -8, atol=1e-6)
 
 
 def test_route_is_deterministic():

@@ -91,3 +91,60 @@ def test_feature_sharded_layer_needs_one_all_reduce():
         assert p.exitcode == 0
     for _, err in got:
         assert err <= 1e-12
+
+
+def _runner_worker(rank, world, port, q):
+    """The package's feature-sharded runner on CPU ranks: each rank slices the
+    weights with shard_weights, computes its partial (the oracle stands in for
+    the GPU's moe_forward_f32), and sharded_forward all-reduces and rounds."""
+    import numpy as np
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from oracle import moe_oracle as O
+    from routing_grouped_expert_gb300 import sharded
+    g = torch.Generator().manual_seed(4)
+    T, H, F, E, k = 20, 16, 256 * world, 4, 2
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(E, H, F, generator=g) / 4).to(torch.bfloat16)
+    W3 = (torch.randn(E, H, F, generator=g) / 4).to(torch.bfloat16)
+    W2 = (torch.randn(E, F, H, generator=g) / 16).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g)
+    W1s, W3s, W2s = sharded.shard_weights(W1, W3, W2, world, rank)
+    assert W1s.shape[2] == F // world and W2s.shape[1] == F // world
+
+    def partial(x_, l_, a, b, c, k_):
+        return torch.from_numpy(O.forward_perm(x_, l_.numpy(), a, b, c, k_)["out"]).float()
+    out = sharded.sharded_forward(x, logits, W1s, W3s, W2s, k, partial=partial,
+                                  cast=lambda t: t.to(torch.bfloat16))
+    full = O.forward_perm(x, logits.numpy(), W1, W3, W2, k)["out"]
+    err = np.abs(out.double().numpy() - full)
+    q.put((rank, float((err / (2.0 ** -8 * np.abs(full) + 1e-6)).max())))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_feature_sharded_runner_on_two_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_runner_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, ratio in got:
+        assert ratio <= 1.0      # fp32 partials summed, rounded to bf16 once
+
+
+def test_feature_slices_are_aligned_and_cover_f():
+    from routing_grouped_expert_gb300 import sharded
+    for F, world in ((2048, 8), (16384, 4), (10752, 2), (256, 2)):
+        cuts = [sharded.feature_slice(F, world, r) for r in range(world)]
+        assert cuts[0][0] == 0 and cuts[-1][1] == F
+        assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
+        assert all((hi - lo) % 128 == 0 for lo, hi in cuts)
+    with pytest.raises(ValueError):
+        sharded.feature_slice(384, 2, 0)
+
