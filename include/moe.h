@@ -390,6 +390,15 @@ moe_status moe_get_device_status(const void* ws, void* stream);
 moe_status moe_diag_wait_timeout(void* ws, size_t ws_bytes, long long limit_ns,
                                  void* stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): the same for the bounded counter
+ * wait with which FC2 waits for a token block's FC1 tiles when the two
+ * overlap, on a counter in `ws` that nothing increments.  Same arguments and
+ * results as moe_diag_wait_timeout.
+ */
+moe_status moe_diag_count_wait_timeout(void* ws, size_t ws_bytes, long long limit_ns,
+                                       void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* moe_status_string(moe_status s);
 

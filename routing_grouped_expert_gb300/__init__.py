@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     load_library,
     moe_combine,
     moe_diag_wait_timeout,
+    moe_diag_count_wait_timeout,
     moe_forward,
     moe_forward_events,
     moe_forward_f32,

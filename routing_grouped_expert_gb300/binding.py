@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_get_device_status": (_I, [_VP, _VP]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_diag_wait_timeout": (_I, [_VP, _SZ, ctypes.c_longlong, _VP]),
+    "moe_diag_count_wait_timeout": (_I, [_VP, _SZ, ctypes.c_longlong, _VP]),
     "moe_workspace_size_train": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_train": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "moe_backward": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP,
@@ -153,6 +154,12 @@ def moe_diag_wait_timeout(ws: Workspace, limit_ns: int) -> None:
     """Make a bounded device wait run out (see include/moe.h)."""
     _check(load_library().moe_diag_wait_timeout(ws.ptr, ws.nbytes, limit_ns, _stream()),
            "moe_diag_wait_timeout")
+
+
+def moe_diag_count_wait_timeout(ws: Workspace, limit_ns: int) -> None:
+    """Make the bounded token-block counter wait run out (see include/moe.h)."""
+    _check(load_library().moe_diag_count_wait_timeout(ws.ptr, ws.nbytes, limit_ns, _stream()),
+           "moe_diag_count_wait_timeout")
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None,

@@ -135,6 +135,7 @@ static_assert(sizeof(Bars) <= 1024, "barrier block too large");
 
 struct Item {
   int e, row0, nrows, mt, nb;   // nb: token blocks of this expert
+  int blk;                      // the token block's index in the whole plan
 };
 
 // Flat tile index -> (expert, first row, rows, feature tile).
@@ -166,6 +167,7 @@ __device__ __forceinline__ Item decode_item(int w, int n_mt, const int32_t* bloc
   it.row0 = beg + b * bsz;
   it.nrows = min(bsz, cnt - b * bsz);
   it.nb = nb;
+  it.blk = b0 + b;
   return it;
 }
 
@@ -283,6 +285,21 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) ones.
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Token-block dependencies between FC1 and FC2 of one forward, which then run
+// as two overlapping launches: FC1 (kDepSignal) lets FC2 launch as soon as it
+// starts, and after the h rows of a tile are stored each of its epilogue warps
+// counts itself in at the tile's token block; FC2 (kDepWait, launched with
+// programmatic stream serialization) waits, before loading a tile's h rows,
+// until its block's count reaches every FC1 tile of the block.  FC1 never
+// waits on FC2, and every FC1 CTA is resident before any FC2 CTA launches
+// (one CTA per SM), so the waits end; each is bounded like the pipeline's.
+enum : int { kDepNone = 0, kDepSignal = 1, kDepWait = 2 };
 
 // kGather: the token rows of the N operand are gathered straight from x
 // ([T, K], token-major) by TMA tile::gather4 loads -- row p of an expert
@@ -300,6 +317,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     void* __restrict__ out_ptr, int ld_out, int m_valid, EpiAux aux,
                     const __grid_constant__ OutMaps outs, StreamK sk,
                     const int32_t* __restrict__ gather_src, int gather_k,
+                    int* __restrict__ blk_done, int blk_target, int dep,
                     int* __restrict__ status) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
   constexpr int kBK = C::kBK;
@@ -321,6 +339,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   const int nkb = K / kBK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
 
+  // FC2 may launch on SMs this grid leaves (it waits per token block)
+  if (dep == kDepSignal) pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -508,6 +528,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           break;
         }
         const Item it = decode_item<kBN>(w, n_mt, block_expert, block_off, offsets);
+        if (dep == kDepWait) {
+          // the block's h rows: stored by every FC1 tile of the block
+          if (!wait_count(blk_done + it.blk, blk_target, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          fence_async_global();   // the TMA loads below see what the acquire saw
+        }
         const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
         const uint32_t bytes = kNumA * C::kABytes + nbox * C::kBBoxBytes;
         const int f0 = it.mt * C::kFeatPerItem;
@@ -770,8 +798,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
       }
       // one 16-column chunk of the accumulator: TMEM -> registers -> epilogue
-      auto chunk = [&](int c0) {
-        uint32_t g[16], g2[16];
+      // one 16-column chunk of the accumulator, already in registers (g: tile
+      // 0 / gate, g2: tile 1 / up) -> epilogue -> global memory
+      auto process = [&](int c0, uint32_t (&g)[16], uint32_t (&g2)[16]) {
         float pg[kNumA][16], pu[kNumA][16];
         if constexpr (kEpi == kEpiSwigluBwd) {
           // all saved g, u of the chunk are loaded first: a load placed after a
@@ -786,9 +815,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
               pu[a][c] = in ? __bfloat162float(aux.u[i]) : 0.f;
             }
         }
-        tmem_ld_32x32b_x16(tb + c0, g);
-        if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
-        tmem_ld_wait();
         if constexpr (kSKCapable) {
           if (other != nullptr) {   // finish a cut tile: add the neighbour's part
 #pragma unroll
@@ -894,21 +920,65 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           }
         }
       };
-      if constexpr (C::kRegions > 0) {
+      auto load = [&](int c0, uint32_t (&g)[16], uint32_t (&g2)[16]) {
+        tmem_ld_32x32b_x16(tb + c0, g);
+        if constexpr (kNumA == 2) tmem_ld_32x32b_x16(tb + kBN + c0, g2);
+      };
+      if constexpr (C::kRegions > 0 && kEpi != kEpiSwigluBwd) {
+        // One accumulator buffer: the next tile's MMAs wait for each 64-column
+        // group.  Read this warp's two chunks of a group into registers, hand
+        // the group back, then convert and store from registers, so the
+        // tensor core waits only for the TMEM reads.
+        for (int r = 0; r < C::kRegions; ++r) {
+          const int c0 = 64 * r + 16 * half, c1 = c0 + 32;
+          const bool l0 = store && c0 < it.nrows, l1 = store && c1 < it.nrows;
+          uint32_t g0[16], h0[16], g1[16], h1[16];
+          if (l0) load(c0, g0, h0);
+          if (l1) load(c1, g1, h1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_region[r]);
+          if (l0) process(c0, g0, h0);
+          if (l1) process(c1, g1, h1);
+        }
+      } else if constexpr (C::kRegions > 0) {
         // hand each 64-column group back as soon as this warp has read it
         for (int r = 0; r < C::kRegions; ++r) {
           for (int c0 = 64 * r + 16 * half; c0 < 64 * r + 64; c0 += 32)
-            if (store && c0 < it.nrows) chunk(c0);
+            if (store && c0 < it.nrows) {
+              uint32_t g[16], g2[16];
+              load(c0, g, g2);
+              tmem_ld_wait();
+              process(c0, g, g2);
+            }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->acc_region[r]);
         }
       } else {
         if (store)
-          for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) chunk(c0);
+          for (int c0 = 16 * half; c0 < it.nrows; c0 += 32) {
+            uint32_t g[16], g2[16];
+            load(c0, g, g2);
+            tmem_ld_wait();
+            process(c0, g, g2);
+          }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+      }
+      if (dep == kDepSignal) {
+        // this warp's part of the tile is in global memory: count it in
+        __threadfence();   // the lanes' direct stores of a partial chunk
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (C::kOuts > 0) bulk_wait_all();   // the TMA stores have completed
+          fence_async_global();
+          __threadfence();
+          atomicAdd(blk_done + it.blk, 1);
+        }
+        __syncwarp();
       }
 
       if (++acc == kAccBufs) {
@@ -1011,8 +1081,12 @@ cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const 
                         int K, long long nb_max, void* out, int ld_out, const EpiAux& aux,
                         const OutMaps& outs, int* status, cudaStream_t s,
                         StreamK sk = StreamK{nullptr, nullptr, 0, nullptr},
-                        Gather gather = Gather{nullptr, 1}) {
+                        Gather gather = Gather{nullptr, 1}, int* blk_done = nullptr,
+                        int blk_target = 0, int dep = kDepNone) {
   using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  // one CTA per SM: a TMEM allocation never waits on another CTA of this or of
+  // an overlapping launch
+  static_assert(C::kSmemBytes > kSmemMax / 2, "one CTA per SM");
   auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kGather>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1031,11 +1105,11 @@ cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const 
     rm.m[0][j] = b.h[j];
     rm.m[1][j] = b1.h[j];
   }
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(a0.m, a1.m, rm, a0.atoms ? 1 : 0, offsets, block_off,
-                                             num_blocks, block_expert, n_mt, K, out, ld_out,
-                                             M_total, aux, outs, sk, gather.sorted_src, gather.k,
-                                             status);
-  return cudaGetLastError();
+  // a waiting launch starts early, on the SMs the previous one leaves
+  return launch_k(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, dep == kDepWait, a0.m,
+                  a1.m, rm, a0.atoms ? 1 : 0, offsets, block_off, num_blocks, block_expert, n_mt,
+                  K, out, ld_out, M_total, aux, outs, sk, gather.sorted_src, gather.k, blk_done,
+                  blk_target, dep, status);
 }
 
 // With 256-row blocks FC2 pairs two adjacent W2 tiles whenever H allows it
@@ -1103,14 +1177,15 @@ template <int kBN, int kBufs1>
 cudaError_t launch_fc1(const WMap& mW1, const WMap& mW3, const RowMap4& mX,
                        const PlanPtrs& pl, int P, int H, int F, int E, __nv_bfloat16* h,
                        const EpiAux* save, int* status, cudaStream_t s, StreamK sk,
-                       const Gather* gather) {
+                       const Gather* gather, int* blk_done) {
   const long long nb_max = max_blocks(P, E, kBN);
+  const int dep = blk_done != nullptr ? kDepSignal : kDepNone;
   OutMaps om;
   if (!map_out(&om.m[0], h, F, P)) return cudaErrorInvalidValue;
   if (gather != nullptr && save == nullptr)
     return launch_gemm<2, kEpiSwiglu, kBN, kBufs1, false, false, true>(
         mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max,
-        h, F, EpiAux{}, om, status, s, sk, *gather);
+        h, F, EpiAux{}, om, status, s, sk, *gather, blk_done, 0, dep);
   if (save != nullptr) {
     if (!map_out(&om.m[1], save->g, save->ld, P) || !map_out(&om.m[2], save->u, save->ld, P))
       return cudaErrorInvalidValue;
@@ -1120,18 +1195,22 @@ cudaError_t launch_fc1(const WMap& mW1, const WMap& mW3, const RowMap4& mX,
   }
   return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(
       mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max, h,
-      F, EpiAux{}, om, status, s, sk);
+      F, EpiAux{}, om, status, s, sk, Gather{nullptr, 1}, blk_done, 0, dep);
 }
 
+// blk_done: wait, per token block, for FC1's tiles of the block (FC1 of this
+// forward ran with the same counters, F / 128 tiles per block).
 template <int kNumA, int kBN, int kBufs>
 cudaError_t launch_fc2(const WMap& mW2, const RowMap4& mH, const PlanPtrs& pl, int P,
                        int H, int F, int E, __nv_bfloat16* y, int* status, cudaStream_t s,
-                       StreamK sk = StreamK{nullptr, nullptr, 0, nullptr}) {
+                       StreamK sk = StreamK{nullptr, nullptr, 0, nullptr},
+                       int* blk_done = nullptr) {
   OutMaps om;
   if (!map_out(&om.m[0], y, H, P)) return cudaErrorInvalidValue;
   return launch_gemm<kNumA, kEpiBf16, kBN, kBufs>(
       mW2, mW2, mH, mH, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, H, F,
-      max_blocks(P, E, kBN), y, H, EpiAux{}, om, status, s, sk);
+      max_blocks(P, E, kBN), y, H, EpiAux{}, om, status, s, sk, Gather{nullptr, 1}, blk_done,
+      (F / BM) * kEpiWarps, blk_done != nullptr ? kDepWait : kDepNone);
 }
 
 // kPairF / kPairH: pair adjacent weight tiles (single-buffered accumulators)
@@ -1180,8 +1259,11 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                const __nv_bfloat16* W3, const __nv_bfloat16* W2, int P, int H,
                                int F, int E, __nv_bfloat16* h, __nv_bfloat16* y, int* status,
                                cudaStream_t s, cudaEvent_t after_fc1, const EpiAux* save,
-                               const StreamKSpace* sks, const GatherRows* gather_rows) {
+                               const StreamKSpace* sks, const GatherRows* gather_rows,
+                               int* blk_done) {
   if (P == 0) return cudaSuccess;
+  // FC2 overlaps FC1 block by block (no event between them, plain forward)
+  if (after_fc1 != nullptr || save != nullptr) blk_done = nullptr;
   const bool gathered = gather_rows != nullptr && save == nullptr;
   const FfnMode mode = ffn_mode(P, E);
   WMap mW1, mW3, mW2;
@@ -1202,27 +1284,35 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
   // fine-grained 1% faster with the queue; uniform blocks -- DBRX, decode --
   // 0.3-1.3% faster in the fixed order).
   const bool queue = mode == FfnMode::kLarge && (long long)P < 2LL * kBlockRowsLarge * E;
+  // FC1 and FC2 draw from queue heads of their own (they may overlap)
   const StreamK sk =
       sks ? StreamK{sks->part, sks->cnt, sks->slot_bytes,
                     queue ? sks->cnt + kStreamKMaxCtas : nullptr}
           : StreamK{nullptr, nullptr, 0, nullptr};
+  StreamK sk2 = sk;
+  if (sk2.queue != nullptr) sk2.queue = sks->cnt + kStreamKMaxCtas + 1;
   cudaError_t err;
   if (mode == FfnMode::kTiny)
-    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp);
+    err = launch_fc1<kBlockRowsTiny, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp,
+                                        blk_done);
   else if (mode == FfnMode::kSmall)
-    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp);
+    err = launch_fc1<kBlockRows, 2>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk, gp,
+                                    blk_done);
   else
     err = launch_fc1<kBlockRowsLarge, 1>(mW1, mW3, mX, pl, P, H, F, E, h, save, status, s, sk,
-                                         gp);
+                                         gp, blk_done);
   if (err != cudaSuccess) return err;
   if (after_fc1 != nullptr && (err = cudaEventRecord(after_fc1, s)) != cudaSuccess) return err;
   if (mode == FfnMode::kTiny)
-    return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
+    return launch_fc2<1, kBlockRowsTiny, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk2,
+                                            blk_done);
   if (mode == FfnMode::kSmall)
-    return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
+    return launch_fc2<1, kBlockRows, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk2, blk_done);
   if (fc2_paired(H))
-    return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
-  return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk);
+    return launch_fc2<2, kBlockRowsLarge, 1>(mW2, mH, pl, P, H, F, E, y, status, s, sk2,
+                                             blk_done);
+  return launch_fc2<1, kBlockRowsLarge, 2>(mW2, mH, pl, P, H, F, E, y, status, s, sk2,
+                                           blk_done);
 }
 
 cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,

@@ -151,7 +151,8 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
                              static_cast<const __nv_bfloat16*>(W1),
                              static_cast<const __nv_bfloat16*>(W3),
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E, h, y, status, s,
-                             ev ? ev[5] : nullptr, save, &sks, gathers ? &gr : nullptr));
+                             ev ? ev[5] : nullptr, save, &sks, gathers ? &gr : nullptr,
+                             pdl ? ws_ptr<int>(ws, L.blk_done) : nullptr));
   if (sh != nullptr)
     MOE_TRY(launch_grouped_ffn(static_cast<const __nv_bfloat16*>(x), sh->plan.offsets,
                                sh->plan.block_off, sh->plan.num_blocks, sh->plan.block_expert,
@@ -241,8 +242,9 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
   int32_t* num_blocks = ws_ptr<int32_t>(ws, L.num_blocks);
   int32_t* block_expert = ws_ptr<int32_t>(ws, L.block_expert);
   const StreamKSpace sks{ws_ptr<float>(ws, L.sk_part), ws_ptr<int>(ws, L.sk_cnt), L.sk_slot};
-  // the status word and FC2's split counters (adjacent) start at zero
-  MOE_TRY(cudaMemsetAsync(status, 0, L.sk_cnt - L.status + kSkCntInts * sizeof(int), s));
+  // the status word, the split counters and queue heads, and the per-block
+  // FC1 counters (adjacent) start at zero
+  MOE_TRY(cudaMemsetAsync(status, 0, L.chunk_base - L.status, s));
   MOE_TRY(launch_plan(offsets, E, P, block_off, num_blocks, block_expert,
                       ffn_block_rows(P, E, H, F), status, s));
   // with small token blocks FC1 gathers the rows of x itself (row p = token
@@ -258,7 +260,7 @@ moe_status moe_grouped_ffn(const void* x, const int32_t* sorted_src, const int32
                              static_cast<const __nv_bfloat16*>(W2), P, H, F, E,
                              ws_ptr<__nv_bfloat16>(ws, L.h),
                              static_cast<__nv_bfloat16*>(y_sorted), status, s, nullptr, nullptr,
-                             &sks, gathers ? &gr : nullptr));
+                             &sks, gathers ? &gr : nullptr, ws_ptr<int>(ws, L.blk_done)));
   return MOE_OK;
 }
 

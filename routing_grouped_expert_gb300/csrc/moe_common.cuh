@@ -78,13 +78,14 @@ __device__ __forceinline__ void set_status(int* status, int code, int detail = 0
 // CTAs whose FC2 partial tiles the workspace has room for (a launch with a
 // larger grid does not split tiles).
 constexpr int kStreamKMaxCtas = 256;
-// The split counters are followed by the grouped GEMM's tile-queue head (one
-// int, padded to 128 bytes); all are zero between launches.
+// The split counters are followed by the grouped GEMM's tile-queue heads (FC1
+// and FC2, one int each, padded to 128 bytes); all are zero between launches.
 constexpr int kSkCntInts = kStreamKMaxCtas + 32;
 
 struct WsLayout {
   size_t status;        // int32[64]
-  size_t sk_cnt;        // int32[kSkCntInts]   split counters, then the tile-queue head (cleared with status)
+  size_t sk_cnt;        // int32[kSkCntInts]   split counters, then the tile-queue heads (cleared with status)
+  size_t blk_done;      // int32[max_blocks]   FC1 tiles done per token block (cleared with status)
   size_t topk_idx;      // int32[P]
   size_t topk_w;        // f32[P]
   size_t counts;        // int32[E]
@@ -142,7 +143,8 @@ inline WsLayout ws_layout(int T, int H, int F, int E, int k) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
   L.status = take(64 * 4);
   L.sk_cnt = take((size_t)kSkCntInts * 4);
-  L.chunk_base = take(C * E * 4);   // after status and sk_cnt: one memset clears all three
+  L.blk_done = take((size_t)max_blocks((long long)P, E, kBlockRowsTiny) * 4 + 4);
+  L.chunk_base = take(C * E * 4);   // after status, sk_cnt, blk_done: one memset clears all
   L.topk_idx = take(P * 4);
   L.topk_w = take(P * 4);
   L.counts = take((size_t)E * 4);
@@ -293,7 +295,10 @@ struct GatherRows {
 // FC1 (+SwiGLU) and FC2 over the expert groups.  FC1's token rows are rows of
 // x_perm (expert order), or, with `gather` (and no `save`), gathered from x
 // by the GEMM's own loads.  With `save`, FC1 also keeps its pre-activations
-// g = x W1, u = x W3 (bf16, [P, F]) for the backward.
+// g = x W1, u = x W3 (bf16, [P, F]) for the backward.  With `blk_done` (one
+// zeroed int per token block, no `after_fc1` event, no `save`) FC2 starts on
+// the SMs FC1 leaves and waits, per token block, only for the FC1 tiles of
+// that block.
 cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                const int32_t* block_off, const int32_t* num_blocks,
                                const int32_t* block_expert, const __nv_bfloat16* W1,
@@ -302,7 +307,8 @@ cudaError_t launch_grouped_ffn(const __nv_bfloat16* x_perm, const int32_t* offse
                                cudaStream_t s, cudaEvent_t after_fc1 = nullptr,
                                const EpiAux* save = nullptr,
                                const StreamKSpace* sks = nullptr,
-                               const GatherRows* gather = nullptr);
+                               const GatherRows* gather = nullptr,
+                               int* blk_done = nullptr);
 // Backward DGrad of both expert GEMMs: dh = dY W2^T -> dg, du (SwiGLU
 // derivative from the saved g, u), dx_perm = dg W1^T + du W3^T.
 cudaError_t launch_dgrad(const __nv_bfloat16* dY, const __nv_bfloat16* g, const __nv_bfloat16* u,

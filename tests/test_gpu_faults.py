@@ -27,6 +27,23 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     assert torch.isfinite(out.float()).all()
 
 
+def test_block_counter_wait_that_runs_out_reports_timeout():
+    """The wait FC2 uses for a token block's FC1 tiles, on a counter nothing
+    increments: MOE_ERR_TIMEOUT after the limit, and the context still works
+    (the overlapped forward right after it is correct and reports OK)."""
+    ws = moe.Workspace()
+    ws.ensure(4096)
+    t0 = time.perf_counter()
+    moe.moe_diag_count_wait_timeout(ws, 20_000_000)    # 20 ms
+    assert moe.moe_get_device_status(ws) == 3          # MOE_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    wl = I.small("after_count_timeout", T=600, H=256, F=512, E=2, k=2)
+    d = {n: t.cuda() for n, t in I.make_inputs(wl, "cpu").items()}
+    out = moe.moe_forward(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], 2, ws=ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.isfinite(out.float()).all()
+
+
 def test_bad_arguments_raise_on_the_host():
     ws = moe.Workspace()
     ws.ensure(4096)
