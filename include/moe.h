@@ -218,6 +218,19 @@ moe_status moe_forward_f32(const void* x, const float* router_logits,
                            int T, int H, int F, int E, int k, float* out,
                            void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * The routing a moe_forward (or moe_forward_f32 / moe_forward_host /
+ * moe_forward_train) call on `ws` with these sizes computed: copies the
+ * layer's own topk_idx [T, k], topk_w [T, k], counts [E], offsets [E+1],
+ * sorted_src [T*k] and dest_of [T*k] (layouts as in moe_route_topk and
+ * moe_permute) out of the workspace, stream-ordered after that call, for
+ * inspecting and testing the fused path.
+ */
+moe_status moe_forward_routing(const void* ws, size_t ws_bytes, int T, int H, int F, int E,
+                               int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                               int32_t* offsets, int32_t* sorted_src, int32_t* dest_of,
+                               void* stream);
+
 /* out[i] = bf16(in[i]) for i < n, round to nearest even: the layer's output
  * from the reduced fp32 partials of moe_forward_f32.  in fp32 [n], out bf16
  * [n], both 16-byte aligned device pointers; no workspace. */

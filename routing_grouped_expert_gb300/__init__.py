@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     moe_forward_events,
     moe_forward_f32,
     moe_cast_bf16,
+    moe_forward_routing,
     moe_forward_stage_name,
     FORWARD_STAGES,
     moe_forward_host,

@@ -48,6 +48,8 @@ SIGNATURES = {
                                _VP, _VP, _SZ, _VP]),
     "moe_forward_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "moe_cast_bf16": (_I, [_VP, _VP, _SZ, _VP]),
+    "moe_forward_routing": (_I, [_VP, _SZ, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 _VP]),
     "moe_plan_workspace_size": (_SZ, [_I, _I]),
     "moe_plan_replicas": (_I, [_VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
 }
@@ -267,6 +269,22 @@ def moe_forward_f32(x, router_logits, W1, W3, W2, k: int, out=None,
                                           H, F, E, k, _p(out), ws.ptr, ws.nbytes, _stream()),
            "moe_forward_f32")
     return out
+
+
+def moe_forward_routing(ws: Workspace, T: int, H: int, F: int, E: int, k: int):
+    """The routing the last layer call on `ws` computed: (topk_idx, topk_w,
+    counts, offsets, sorted_src, dest_of) copied out of the workspace."""
+    dev = ws.device
+    outs = (torch.empty(T, k, dtype=torch.int32, device=dev),
+            torch.empty(T, k, dtype=torch.float32, device=dev),
+            torch.empty(E, dtype=torch.int32, device=dev),
+            torch.empty(E + 1, dtype=torch.int32, device=dev),
+            torch.empty(T * k, dtype=torch.int32, device=dev),
+            torch.empty(T * k, dtype=torch.int32, device=dev))
+    _check(load_library().moe_forward_routing(ws.ptr, ws.nbytes, T, H, F, E, k,
+                                              *[_p(t) for t in outs], _stream()),
+           "moe_forward_routing")
+    return outs
 
 
 def moe_cast_bf16(x: torch.Tensor, out=None):

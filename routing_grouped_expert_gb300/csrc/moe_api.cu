@@ -309,6 +309,30 @@ moe_status moe_forward_f32(const void* x, const float* router_logits, const void
                         /*out_f32=*/true);
 }
 
+moe_status moe_forward_routing(const void* ws, size_t ws_bytes, int T, int H, int F, int E,
+                               int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                               int32_t* offsets, int32_t* sorted_src, int32_t* dest_of,
+                               void* stream) {
+  if (!ok_sizes(T, H, F, E, k)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!ok_ptr(topk_idx) || !ok_ptr(topk_w) || !ok_ptr(counts) || !ok_ptr(offsets) ||
+      !ok_ptr(sorted_src) || !ok_ptr(dest_of))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(const_cast<void*>(ws), ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t P = (size_t)T * k;
+  const char* w = static_cast<const char*>(ws);
+  const cudaMemcpyKind d2d = cudaMemcpyDeviceToDevice;
+  MOE_TRY(cudaMemcpyAsync(topk_idx, w + L.topk_idx, P * 4, d2d, s));
+  MOE_TRY(cudaMemcpyAsync(topk_w, w + L.topk_w, P * 4, d2d, s));
+  MOE_TRY(cudaMemcpyAsync(counts, w + L.counts, (size_t)E * 4, d2d, s));
+  MOE_TRY(cudaMemcpyAsync(offsets, w + L.offsets, (size_t)(E + 1) * 4, d2d, s));
+  MOE_TRY(cudaMemcpyAsync(sorted_src, w + L.sorted_src, P * 4, d2d, s));
+  MOE_TRY(cudaMemcpyAsync(dest_of, w + L.dest_of, P * 4, d2d, s));
+  return MOE_OK;
+}
+
 moe_status moe_cast_bf16(const float* in, void* out, size_t n, void* stream) {
   if (n == 0) return MOE_OK;
   if (!ok_ptr(in) || !ok_ptr(out) || n >= ((size_t)1 << 40)) return MOE_ERR_INVALID_ARG;

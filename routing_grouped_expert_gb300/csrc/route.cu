@@ -7,26 +7,12 @@
 // value wins, equal values (IEEE ==, so -0.0 ties +0.0) go to the lower
 // expert index.  The weights are the softmax over the k selected logits,
 // in fp32 with the largest selected logit subtracted first.
-#include <math.h>
-
-#include "moe_common.cuh"
+#include "route_token.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;   // 8 warps, one token each
-
-struct Cand {
-  float v;
-  int i;   // expert index, -1 = no candidate
-};
-
-// True when candidate b should replace a.
-__device__ __forceinline__ bool better(const Cand& b, const Cand& a) {
-  if (b.i < 0) return false;
-  if (a.i < 0) return true;
-  return b.v > a.v || (b.v == a.v && b.i < a.i);
-}
 
 template <int kPerLane>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -39,57 +25,17 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int tpc
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * (kRouteThreads / 32) + warp;   // one token per warp
   if (t >= T) return;
-  const float* row = logits + (size_t)t * E;
-  bool nonfinite = false;
-  float v[kPerLane];
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    const int e = lane + 32 * i;
-    float x = (e < E) ? __ldg(row + e) : -INFINITY;
-    if (e < E && !isfinite(x)) {
-      nonfinite = true;
-      if (isnan(x)) x = -INFINITY;   // keep the order total; status reports it
-    }
-    v[i] = x;
-  }
-  uint32_t taken = 0;
-  float my_sel = 0.f;
-  int my_idx = 0;
-  for (int j = 0; j < k; ++j) {
-    Cand c{-INFINITY, -1};
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        Cand d{v[i], e};
-        if (better(d, c)) c = d;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      Cand o{__shfl_xor_sync(0xffffffffu, c.v, off), __shfl_xor_sync(0xffffffffu, c.i, off)};
-      if (better(o, c)) c = o;
-    }
-    if (c.i >= 0 && (c.i & 31) == lane) taken |= 1u << (c.i >> 5);
-    if (lane == j) {
-      my_sel = c.v;
-      my_idx = c.i;
-    }
-  }
-  // softmax over the k selected logits (slot 0 holds the largest)
-  const float m = __shfl_sync(0xffffffffu, my_sel, 0);
-  float ex = (lane < k) ? expf(my_sel - m) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  int my_idx;
+  float my_w;
+  const bool nonfinite = route_token<kPerLane>(logits + (size_t)t * E, E, k, lane, &my_idx, &my_w);
   if (lane < k) {
     topk_idx[(size_t)t * k + lane] = my_idx;
-    topk_w[(size_t)t * k + lane] = ex / sum;
+    topk_w[(size_t)t * k + lane] = my_w;
     // integer counts: the order of the atomic adds does not change them
     if (chunk_hist && my_idx >= 0 && my_idx < E)
       atomicAdd(&chunk_hist[(size_t)(t / tpc) * E + my_idx], 1);
   }
-  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  if (nonfinite && lane == 0) set_status(status, MOE_ERR_NONFINITE);
 }
 
 // Per-chunk histogram of a caller-supplied topk_idx (moe_permute on its own).

@@ -135,3 +135,27 @@ def test_route_is_deterministic():
     pb = moe.moe_permute(b[0], 256)
     for x, y in zip(pa, pb):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (96, 8, 2), (256, 8, 2), (2048, 8, 2),
+                                   (512, 256, 8), (4096, 16, 1), (33, 37, 5), (4100, 16, 1),
+                                   (600, 300, 4)])
+def test_forward_routing_bit_exact(T, E, k):
+    """The routing moe_forward itself computed, copied out of the workspace,
+    against the oracle: bit-exact indices and permutation."""
+    from routing_grouped_expert_gb300 import inputs as I
+    wl = I.small("routing", T=T, H=128, F=128, E=E, k=k)
+    d = {n: t.cuda() for n, t in I.make_inputs(wl, "cpu").items()}
+    for kind in ("normal", "ties"):
+        logits = logits_for(T, E, kind, seed=T + E + k).float()
+        ws = moe.Workspace()
+        moe.moe_forward(d["x"], logits.cuda(), d["W1"], d["W3"], d["W2"], k, ws=ws)
+        assert moe.moe_get_device_status(ws) == 0
+        idx, w, counts, off, src, dest = moe.moe_forward_routing(ws, T, 128, 128, E, k)
+        idx_ref, w_ref = O.route_topk(logits.numpy(), k)
+        np.testing.assert_array_equal(to_np(idx), idx_ref)
+        np.testing.assert_allclose(to_np(w), w_ref, rtol=0, atol=W_ATOL)
+        for name, got, ref in zip(("counts", "offsets", "sorted_src", "dest_of"),
+                                  (counts, off, src, dest), O.permute(idx_ref, E)):
+            np.testing.assert_array_equal(to_np(got), ref, err_msg=f"{name} {kind}")
+
