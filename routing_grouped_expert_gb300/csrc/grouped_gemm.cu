@@ -68,8 +68,12 @@ enum : int {
 // kAKMajor: the weight tile is read K-major (the backward's W^T products)
 // instead of MN-major.  kDualK: the K loop runs twice, first over
 // (A0, B0) then over (A1, B1), into one accumulator (dx = dg W1^T + du W3^T).
+// kPair: two CTAs of a cluster compute one tile of twice the features (M =
+// 256 per MMA, .cta_group::2); each stages its own weight tiles and half of
+// the token block (kBN / 2 rows), so the stages are smaller and the ring
+// deeper (FC1: four stages of 48 KB instead of three of 64 KB).
 template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false,
-          bool kDualK = false>
+          bool kDualK = false, bool kPair = false>
 struct Cfg {
   static constexpr bool kGLU = kEpi == kEpiSwiglu || kEpi == kEpiSwigluSave;
   static constexpr int kBK = BK;
@@ -77,7 +81,8 @@ struct Cfg {
   static constexpr int kABytes = BM * kBK * 2;          // one 128-feature weight tile
   static constexpr int kRowBytes = kBK * 2;             // one token row of the N operand
   static constexpr int kBBoxBytes = kRowBox * kRowBytes;   // 32 token rows
-  static constexpr int kBBytes = kBN * kRowBytes;
+  static constexpr int kBRows = kPair ? kBN / 2 : kBN;      // token rows staged by this CTA
+  static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes;
   // bf16 outputs per accumulator column: each leaves through a 16-row x
   // 32-feature staging box (1 KB per warp) and a TMA store
@@ -111,9 +116,14 @@ struct Cfg {
   static_assert(!kGLU || kNumA == 2, "SwiGLU needs the gate and up tiles");
   static_assert(kEpi != kEpiF32 || kNumA == 1, "single tile");
   static_assert(!kDualK || kAKMajor, "two-phase K: K-major weight tiles");
+  // pairs: FC1 of the forward (SwiGLU, one accumulator buffer), 256-row blocks
+  static_assert(!kPair || (kEpi == kEpiSwiglu && kBN == 256 && kAccBufs == 1 && !kAKMajor &&
+                           !kDualK),
+                "CTA pairs: forward FC1 with 256-row blocks");
 };
 
 constexpr int kSegRing = 4;   // segments the producer may run ahead of the other roles
+
 
 struct Bars {
   uint64_t full[8];
@@ -204,18 +214,20 @@ struct Segments {
   int w, step, nkb, round_robin_end;
   bool sk, drawn_past = false;
   int* queue;
-  __device__ Segments(bool split_ok, int total, int nkb_, int* queue_)
-      : step(gridDim.x), nkb(nkb_), queue(queue_) {
-    const int G = gridDim.x;
+  // `cta` of `ctas`: this CTA's place among the tile takers (a CTA pair
+  // takes its tiles together, as one)
+  __device__ Segments(bool split_ok, int total, int nkb_, int* queue_, int cta, int ctas)
+      : step(ctas), nkb(nkb_), queue(queue_) {
+    const int G = ctas;
     sk = split_ok && total > G && total % G != 0;
     round_robin_end = sk ? (total / G - 1) * G : total;
     // the split assumes every CTA takes the same number of whole tiles: fixed order
     if (sk) queue = nullptr;
     const long long base = (long long)round_robin_end * nkb;
     const long long U = (long long)(total - round_robin_end) * nkb;
-    u = base + U * blockIdx.x / G;
-    end = base + U * (blockIdx.x + 1) / G;
-    w = queue ? atomicAdd(queue, 1) : (int)blockIdx.x;
+    u = base + U * cta / G;
+    end = base + U * (cta + 1) / G;
+    w = queue ? atomicAdd(queue, 1) : cta;
   }
   __device__ bool next(int& wo, int& kb0, int& kb1) {
     if (w < round_robin_end) {
@@ -227,7 +239,7 @@ struct Segments {
     }
     if (queue && !drawn_past) {   // this CTA's one draw past the whole tiles
       drawn_past = true;
-      if (w == round_robin_end + (int)gridDim.x - 1) atomicExch(queue, 0);
+      if (w == round_robin_end + step - 1) atomicExch(queue, 0);
     }
     if (!sk || u >= end) return false;
     wo = (int)(u / nkb);
@@ -306,7 +318,23 @@ enum : int { kDepNone = 0, kDepSignal = 1, kDepWait = 2 };
 // group is token sorted_src[p] / k -- so no expert-ordered copy of x is made
 // (FC1 of the forward).  rows.m[0][0] is then a tensor map of x with boxes of
 // one row x 64 K; the producer warp's lanes each gather four rows at a time.
-template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK, bool kGather>
+//
+// kPair: the CTAs run as clusters of two (see Cfg).  A pair takes the tiles
+// of the list as one: tile (expert, block, m) covers features [2m, 2m + 2) x
+// kFeatPerItem, rank r of the pair the r-th half.  Rank r stages the block's
+// rows [r hb, r hb + hb), hb = rows rounded up to 32, halved (N = 2 hb, a
+// multiple of 32).  Rank 0 waits for
+// both halves of a stage (its full barrier counts both ranks' bytes), issues
+// the MMAs and signals stage release, accumulator ready and drain on the
+// barriers of both ranks; each rank reads its own accumulator, stores its own
+// features and hands the accumulator back to rank 0.  Each MMA spans the whole
+// block (N = 2 hb): its first hb columns come from rank 0's rows and the rest
+// from rank 1's, so accumulator column c holds block row c on both ranks.
+// (Measured: splitting the block into MMAs of N = 128 or 64, which would let
+// the next tile start on the columns already read, makes every pair MMA cost
+// about as much as a full one -- the fine-grained FC1 1.4x and 2.2x slower.)
+template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor, bool kDualK, bool kGather,
+          bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -319,9 +347,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const int32_t* __restrict__ gather_src, int gather_k,
                     int* __restrict__ blk_done, int blk_target, int dep,
                     int* __restrict__ status) {
-  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kPair>;
   constexpr int kBK = C::kBK;
   static_assert(!kGather || (!kDualK && !kAKMajor), "gathered rows: forward products only");
+  static_assert(!kPair || !kGather, "CTA pairs: rows staged by plain tile loads");
   constexpr bool kGLU = C::kGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -335,7 +364,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
   // the next tile's MMAs, and FC1 prefers every CTA on neighbouring tiles.
   constexpr bool kSKCapable = kEpi == kEpiBf16 && kNumA == 1 && kAccBufs == 2;
   constexpr size_t kSlot = (size_t)kNumA * BM * kBN;   // floats of one partial tile
-  const bool sk_ok = kSKCapable && sk.part != nullptr;
+  const bool sk_ok = kSKCapable && !kPair && sk.part != nullptr;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // within the pair
   const int nkb = K / kBK;                        // K stages per phase
   const int nkb_all = kDualK ? 2 * nkb : nkb;
 
@@ -354,7 +384,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       mbar_init(&bars->acc_full[b], 1);
       mbar_init(&bars->acc_empty[b], kEpiWarps);   // one arrival per epilogue warp
     }
-    for (int r = 0; r < C::kRegions; ++r) mbar_init(&bars->acc_region[r], kEpiWarps);
+    // pairs: rank 0's group barriers count both ranks' epilogue warps
+    for (int r = 0; r < C::kRegions; ++r)
+      mbar_init(&bars->acc_region[r], (kPair ? 2 : 1) * kEpiWarps);
     mbar_init(&bars->sk_written, kEpiWarps);
     mbar_init(&bars->sk_decided, 1);
     mbar_init(&bars->drain, 1);
@@ -368,14 +400,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       for (int j = 0; j < 4; ++j) prefetch_tmap(&rows.m[ph][j]);
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&bars->tmem_base, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  // pairs: both ranks' barriers are initialised before either signals the other's
+  if constexpr (kPair) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
+  // A role that gives up stops the other roles of its CTA and of its pair.
+  auto raise_abort = [=]() {
+    *abort_flag = 1;
+    if constexpr (kPair)
+      st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&bars->abort)), rank ^ 1u), 1u);
+  };
 
   if (warp == 0 && kGather) {
     // ----------------------------------- TMA producer, gathered token rows
@@ -391,7 +435,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     uint32_t phase = 0;
     bool ok = true;
     // only lane 0 draws from the queue; the other lanes' copies stay idle
-    Segments sg(sk_ok, total, nkb_all, lane == 0 ? sk.queue : nullptr);
+    Segments sg(sk_ok, total, nkb_all, lane == 0 ? sk.queue : nullptr, (int)blockIdx.x,
+                (int)gridDim.x);
     int sslot = 0;
     uint32_t sphase = 0;
     while (true) {
@@ -487,7 +532,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       }
       if (!ok) {
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailProducer);
-        *abort_flag = 1;
+        raise_abort();
       }
       // No TMA write may land after the CTA exits: wait for the last loads.
       for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
@@ -506,7 +551,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      Segments sg(sk_ok, total, nkb_all, sk.queue);
+      // a pair takes its tiles in the fixed order (both ranks the same ones)
+      Segments sg(sk_ok, total, nkb_all, kPair ? nullptr : sk.queue,
+                  kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x,
+                  kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x);
       int w, kb0, kb1;
       int sslot = 0;
       uint32_t sphase = 0;
@@ -536,9 +584,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           }
           fence_async_global();   // the TMA loads below see what the acquire saw
         }
-        const int nbox = (it.nrows + kRowBox - 1) / kRowBox;
+        // this CTA's token rows [rb0, rb0 + nr) of the block (pairs: its half)
+        const int hb = kPair ? ((it.nrows + 31) & ~31) / 2 : 0;
+        const int rb0 = kPair ? (int)rank * hb : 0;
+        const int nr = kPair ? hb : it.nrows;
+        const int nbox = (nr + kRowBox - 1) / kRowBox;
         const uint32_t bytes = kNumA * C::kABytes + nbox * C::kBBoxBytes;
-        const int f0 = it.mt * C::kFeatPerItem;
+        const int f0 = (kPair ? 2 * it.mt + (int)rank : it.mt) * C::kFeatPerItem;
         const uint64_t pol_w = it.nb > 1 ? pol_shared : pol_once;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -550,6 +602,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + kNumA * C::kABytes;
           uint64_t* fb = &bars->full[stage];
+          if constexpr (kPair) {
+            // rank 0's full barrier counts both ranks' bytes (equal halves)
+            const uint32_t fbc = mapa_shared(smem_u32(fb), 0);
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * bytes);
+#pragma unroll
+            for (int a = 0; a < kNumA; ++a) {
+              const CUtensorMap* map = (kGLU && a == 1) ? &tmA1 : &tmA0;
+              const int fa = f0 + (kGLU ? 0 : a * BM);
+              if (a_atoms) {
+                tma_load_4d_pair(sA + a * C::kABytes, map, fbc, 0, k0, fa >> 6, it.e, pol_w);
+              } else {
+                tma_load_3d_pair(sA + a * C::kABytes, map, fbc, fa, k0, it.e, pol_w);
+                tma_load_3d_pair(sA + a * C::kABytes + C::kAHalfBytes, map, fbc, fa + 64, k0,
+                                 it.e, pol_w);
+              }
+            }
+            for (int r = 0; r < nbox * kRowBox;) {
+              const int rem = nbox * kRowBox - r;
+              const int lg = (C::kBRows >= 128 && rem >= 128) ? 2 : rem >= 64 ? 1 : 0;
+              tma_load_2d_pair(sB + r * C::kRowBytes, &rows.m[0][lg], fbc, k0,
+                               it.row0 + rb0 + r, pol_x);
+              r += kRowBox << lg;
+            }
+            ++issued;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
           for (int a = 0; a < kNumA; ++a) {
@@ -588,12 +670,44 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       if (ok) ok = publish(-1, 0, 0);
       if (!ok) {
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailProducer);
-        *abort_flag = 1;
+        raise_abort();
       }
-      // No TMA write may land after the CTA exits: wait for the last loads.
-      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
-        mbar_wait(&bars->full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), nullptr,
-                  kWaitLimitNs);
+      // No TMA write may land after the CTA exits: wait for the last loads
+      // (pairs: rank 0's barriers count rank 1's loads too, and rank 1 does
+      // not leave before rank 0 -- the cluster barrier at the end).
+      if (!kPair || rank == 0)
+        for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+          mbar_wait(&bars->full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), nullptr,
+                    kWaitLimitNs);
+    }
+  } else if (warp == 1 && kPair && rank != 0) {
+    // ------------------------------------- pair rank 1: no MMAs of its own
+    // It takes the segments (the producer's ring counts this warp) and waits
+    // until rank 0's MMAs, which read its shared memory and write its tensor
+    // memory, have drained.
+    if (lane == 0) {
+      bool ok = true;
+      int sslot = 0;
+      uint32_t sphase = 0;
+      while (true) {
+        if (!mbar_wait(&bars->seg_full[sslot], sphase, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int x = bars->seg[sslot].x;
+        mbar_arrive(&bars->seg_empty[sslot]);
+        if (++sslot == kSegRing) {
+          sslot = 0;
+          sphase ^= 1u;
+        }
+        if (x < 0) break;
+      }
+      if (!ok) {
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailMma);
+        raise_abort();
+      }
+      if (!mbar_wait(&bars->drain, 0, nullptr, kWaitLimitNs))
+        set_status(status, MOE_ERR_TIMEOUT, kWaitDetailDrain);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
@@ -636,6 +750,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           tc_fence_after();
           const uint32_t a0 = sbase + (uint32_t)(stage * C::kStageBytes);
           const uint32_t b0 = a0 + (uint32_t)(kNumA * C::kABytes);
+          if constexpr (kPair) {
+            // one MMA per K step and weight tile over the whole block
+            if (C::kRegions > 0 && kb == kb0) {   // the previous tile's epilogue is done
+              for (int r = 0; ok && r < C::kRegions; ++r)
+                ok = mbar_wait(&bars->acc_region[r], acc_phase ^ 1u, abort_flag, kWaitLimitNs);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const int np = (it.nrows + 31) & ~31;
+            const uint32_t idesc_p = idesc_bf16(2 * BM, np, /*a_mn=*/true, /*b_mn=*/false);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t db = sdesc_sw128(b0 + kk * 32, 16, 1024);
+#pragma unroll
+              for (int a = 0; a < kNumA; ++a) {
+                const uint64_t da =
+                    sdesc_sw128(a0 + a * C::kABytes + kk * 2048, C::kAHalfBytes, 1024);
+                mma_bf16_ss_pair(d0 + (uint32_t)(a * kBN), da, db, idesc_p,
+                                 (kb > kb0 || kk) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
+            mma_commit_pair(&bars->empty[stage], 0x3);
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (C::kRegions > 0 && kb == kb0) {
             // First stage, one 64-token-column group at a time, each once the
             // epilogue has read it out of the previous tile.  Per accumulator
@@ -689,7 +832,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           }
         }
         if (!ok) break;
-        mma_commit(&bars->acc_full[acc]);
+        if constexpr (kPair) mma_commit_pair(&bars->acc_full[acc], 0x3);
+        else mma_commit(&bars->acc_full[acc]);
         if (++acc == kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
@@ -697,10 +841,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       }
       if (!ok) {
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailMma);
-        *abort_flag = 1;
+        raise_abort();
       }
-      // Every MMA issued so far completes before TMEM is released.
-      mma_commit(&bars->drain);
+      // Every MMA issued so far completes before TMEM is released (pairs:
+      // rank 1 waits for the same on its own drain barrier).
+      if constexpr (kPair) mma_commit_pair(&bars->drain, 0x3);
+      else mma_commit(&bars->drain);
       if (!mbar_wait(&bars->drain, 0, nullptr, kWaitLimitNs))
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailDrain);
     }
@@ -738,7 +884,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         break;
       }
       tc_fence_after();
-      const int wfeat = it.mt * C::kFeatPerItem + q * 32;   // the warp's first feature
+      // the warp's first feature (pairs: rank r stores the r-th half of the tile)
+      const int wfeat = (kPair ? 2 * it.mt + (int)rank : it.mt) * C::kFeatPerItem + q * 32;
       const int feat = wfeat + lane;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       // A tile cut between two CTAs: store this part, count in at the boundary;
@@ -938,7 +1085,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->acc_region[r]);
+          if (lane == 0) {   // pairs: on rank 0's barrier
+            if (kPair && rank != 0)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_region[r]), 0));
+            else
+              mbar_arrive(&bars->acc_region[r]);
+          }
           if (l0) process(c0, g0, h0);
           if (l1) process(c1, g1, h1);
         }
@@ -990,16 +1142,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
       if constexpr (C::kOuts > 0) bulk_wait_all();   // every staged box written
       if (!ok) {
         set_status(status, MOE_ERR_TIMEOUT, kWaitDetailEpilogue);
-        *abort_flag = 1;
+        raise_abort();
       }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  // pairs: neither rank leaves (or frees its tensor memory) while the other
+  // may still read its shared memory, signal its barriers or write its TMEM
+  if constexpr (kPair) cluster_sync(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -1073,8 +1228,52 @@ struct Gather {
   int k;
 };
 
+// Clusters of two CTAs of `kern` that fit on the device at once (each CTA
+// alone on its SM); 0 if the query fails.
+template <typename Kern>
+int pair_clusters(Kern kern, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * device_sm_count());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// As launch_k, as clusters of two CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pair_k(void (*kern)(KArgs...), int grid, size_t smem, cudaStream_t s,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int kNumA, int kEpi, int kBN, int kAccBufs, bool kAKMajor = false, bool kDualK = false,
-          bool kGather = false>
+          bool kGather = false, bool kPair = false>
 cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const RowMap4& b1,
                         const int32_t* offsets, const int32_t* block_off,
                         const int32_t* num_blocks, const int32_t* block_expert, int M_total,
@@ -1083,14 +1282,30 @@ cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const 
                         StreamK sk = StreamK{nullptr, nullptr, 0, nullptr},
                         Gather gather = Gather{nullptr, 1}, int* blk_done = nullptr,
                         int blk_target = 0, int dep = kDepNone) {
-  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK>;
+  using C = Cfg<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kPair>;
   // one CTA per SM: a TMEM allocation never waits on another CTA of this or of
   // an overlapping launch
   static_assert(C::kSmemBytes > kSmemMax / 2, "one CTA per SM");
-  auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kGather>;
+  auto kern = grouped_gemm_kernel<kNumA, kEpi, kBN, kAccBufs, kAKMajor, kDualK, kGather, kPair>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
+  if constexpr (kPair) {
+    // a pair's tile covers 2 kFeatPerItem features (M_total a multiple of it);
+    // one pair per two SMs, as many as are resident at once
+    static const int clusters = pair_clusters(kern, C::kSmemBytes);
+    if (clusters <= 0 || M_total % (2 * C::kFeatPerItem) != 0) return cudaErrorInvalidValue;
+    const int n_mt = M_total / (2 * C::kFeatPerItem);
+    const long long items = nb_max * n_mt;
+    const int grid = 2 * (int)(items < clusters ? items : clusters);
+    RowMaps rm;
+    for (int j = 0; j < 4; ++j) rm.m[0][j] = rm.m[1][j] = b.h[j];
+    const StreamK none{nullptr, nullptr, 0, nullptr};
+    return launch_pair_k(kern, grid, C::kSmemBytes, s, dep == kDepWait, a0.m, a1.m, rm,
+                         a0.atoms ? 1 : 0, offsets, block_off, num_blocks, block_expert, n_mt,
+                         K, out, ld_out, M_total, aux, outs, none, gather.sorted_src, gather.k,
+                         blk_done, blk_target, dep, status);
+  }
   // a partial last feature tile (router with E not a multiple of 128) is
   // zero-filled by the TMA and not stored
   const int n_mt = (M_total + C::kFeatPerItem - 1) / C::kFeatPerItem;
@@ -1115,6 +1330,16 @@ cudaError_t launch_gemm(const WMap& a0, const WMap& a1, const RowMap4& b, const 
 // With 256-row blocks FC2 pairs two adjacent W2 tiles whenever H allows it
 // (measured faster than unpaired, double-buffered tiles on every large shape).
 bool fc2_paired(int H) { return H % (2 * BM) == 0; }
+// FC1 of the plain forward runs on CTA pairs (two SMs per tile, a four-stage
+// ring) when the features split into pair tiles of 256 and the experts hold
+// fewer than two 256-row blocks on average, where FC1 streams each weight
+// tile once and is bound by HBM (measured: fine-grained layer 4.98 -> 4.88 ms).
+// Where blocks share weight tiles FC1 is bound by the tensor core, and a pair
+// MMA costs more than two single ones (DBRX-sized layer 3.83 -> 4.02 ms); FC2
+// (32-stage tiles) gains nothing from the deeper ring either way.
+bool ffn_paired_fc1(long long P, int E, int F) {
+  return F % (2 * BM) == 0 && P < 2LL * kBlockRowsLarge * E;
+}
 
 struct PlanPtrs {
   const int32_t* offsets;
@@ -1192,6 +1417,12 @@ cudaError_t launch_fc1(const WMap& mW1, const WMap& mW3, const RowMap4& mX,
     return launch_gemm<2, kEpiSwigluSave, kBN, kBufs1>(
         mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max,
         h, F, *save, om, status, s, sk);
+  }
+  if constexpr (kBN == kBlockRowsLarge && kBufs1 == 1) {
+    if (ffn_paired_fc1(P, E, F))
+      return launch_gemm<2, kEpiSwiglu, kBN, kBufs1, false, false, false, true>(
+          mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H,
+          nb_max, h, F, EpiAux{}, om, status, s, sk, Gather{nullptr, 1}, blk_done, 0, dep);
   }
   return launch_gemm<2, kEpiSwiglu, kBN, kBufs1>(
       mW1, mW3, mX, mX, pl.offsets, pl.block_off, pl.num_blocks, pl.block_expert, F, H, nb_max, h,
