@@ -322,7 +322,9 @@ moe_status moe_backward(const void* dout, const float* router_logits,
  * first kernel and events[i] after stage i, for the MOE_FORWARD_STAGES
  * stages route, scan, scatter, gather, fc1, fc2, combine (in that order; the
  * gather stage is empty when the token blocks are small -- T*k <= 40 E -- and
- * FC1 gathers the rows of x it needs itself).
+ * FC1 gathers the rows of x it needs itself; the scan and scatter stages are
+ * empty for small batches -- T*k <= 1024 and E <= 256 -- where one kernel
+ * routes, counts, scans and scatters).
  * `events` points to MOE_FORWARD_STAGES + 1 cudaEvent_t created by the
  * caller.  Same arguments, work and results as moe_forward.
  */

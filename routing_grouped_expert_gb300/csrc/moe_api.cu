@@ -130,12 +130,23 @@ moe_status forward_device(const void* x, const float* logits, const void* W1, co
     MOE_TRY(cudaMemsetAsync(status, 0,
                             L.chunk_base - L.status + (size_t)C * E * sizeof(int32_t), s));
   MOE_TRY(mark(0));
-  MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
-  MOE_TRY(mark(1));
-  MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
-                      ffn_block_rows(P, E, H, F), s, pdl));
-  MOE_TRY(mark(2));
-  MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, offsets, sorted_src, dest_of, s, pdl));
+  if (route_permute_small_ok(T, E, k)) {
+    // small batches: routing, counts, scan, block plan and scatter in one
+    // launch (the scan and scatter stages are then empty); its ticket
+    // counter is the first int of the zeroed chunk table
+    MOE_TRY(launch_route_permute_small(logits, T, E, k, ffn_block_rows(P, E, H, F), topk_idx,
+                                       topk_w, counts, offsets, block_off, num_blocks,
+                                       block_expert, sorted_src, dest_of, chunk, status, s));
+    MOE_TRY(mark(1));
+    MOE_TRY(mark(2));
+  } else {
+    MOE_TRY(launch_route(logits, T, E, k, topk_idx, topk_w, chunk, status, s));
+    MOE_TRY(mark(1));
+    MOE_TRY(launch_scan(chunk, C, E, counts, offsets, block_off, num_blocks, block_expert,
+                        ffn_block_rows(P, E, H, F), s, pdl));
+    MOE_TRY(mark(2));
+    MOE_TRY(launch_scatter(topk_idx, T, E, k, chunk, offsets, sorted_src, dest_of, s, pdl));
+  }
   MOE_TRY(mark(3));
   // With small token blocks FC1 gathers its rows from x itself; otherwise (and
   // in the forward with saves, whose rows the backward's WGrad reads) they are

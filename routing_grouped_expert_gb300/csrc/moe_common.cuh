@@ -241,6 +241,20 @@ cudaError_t launch_count(const int32_t* topk_idx, int T, int E, int k, int32_t* 
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
                         int beta, cudaStream_t s, bool pdl = false);
+// Small batches: route, counts, scan, block plan and scatter in one launch
+// instead of three, same results.  `ticket` is an int that holds zero
+// between launches (the kernel leaves it zero).
+constexpr int kSmallRouteAssign = 1024;
+constexpr int kSmallRouteExperts = 256;
+inline bool route_permute_small_ok(int T, int E, int k) {
+  return (long long)T * k <= kSmallRouteAssign && E <= kSmallRouteExperts;
+}
+cudaError_t launch_route_permute_small(const float* logits, int T, int E, int k, int beta,
+                                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                      int32_t* offsets, int32_t* block_off, int32_t* num_blocks,
+                                      int32_t* block_expert, int32_t* sorted_src,
+                                      int32_t* dest_of, int* ticket, int* status,
+                                      cudaStream_t s);
 // Out-of-range expert indices take no position: dest_of = -1 for them and
 // sorted_src[offsets[E] .. T*k) = -1.
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,

@@ -12,6 +12,7 @@
 //   scatter     : rank of each assignment among equal experts inside its
 //                 chunk (warp match + per-warp counts), base + rank.
 #include "moe_common.cuh"
+#include "route_token.cuh"
 
 namespace moe {
 namespace {
@@ -174,6 +175,99 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int P, int E, int chunk_ass
   if (threadIdx.x < chunk_assign && a < P && a >= offsets[E]) sorted_src[a] = -1;
 }
 
+// Small batches (T*k <= kSmallRouteAssign, E <= kSmallRouteExperts): routing,
+// counts, scan, block plan and the stable scatter in one launch, with the
+// same results as the route, scan and scatter kernels.  Every CTA routes 32
+// tokens (one per warp, as the route kernel); the CTA that finishes last --
+// each takes a ticket from a counter after a fence, and the last ticket
+// holder goes on, so no CTA waits for another -- counts, scans and
+// scatters all T*k assignments: thread a ranks assignment a among the equal
+// experts of its warp (warp match), and the per-warp counts give each warp's
+// base inside the expert, i.e. ascending a within every expert, as in the
+// chunked kernels.  It then zeroes the counter for the next launch.
+constexpr int kSmallRouteThreads = 1024;
+
+template <int kPerLane>
+__global__ void __launch_bounds__(kSmallRouteThreads)
+route_permute_small_kernel(const float* __restrict__ logits, int T, int E, int k, int beta,
+                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                           int32_t* __restrict__ block_off, int32_t* __restrict__ num_blocks,
+                           int32_t* __restrict__ block_expert, int32_t* __restrict__ sorted_src,
+                           int32_t* __restrict__ dest_of, int* __restrict__ ticket,
+                           int* __restrict__ status) {
+  __shared__ int cnt[32 * kSmallRouteExperts];   // [warp][expert]: count, then base
+  __shared__ int off_s[kSmallRouteExperts];
+  __shared__ int warp_sums[33];
+  __shared__ int last;
+  // first kernel of the fused chain (launched in stream order)
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * (kSmallRouteThreads / 32) + warp;
+  if (t < T) {
+    int my_idx;
+    float my_w;
+    const bool nonfinite =
+        route_token<kPerLane>(logits + (size_t)t * E, E, k, lane, &my_idx, &my_w);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_idx;
+      topk_w[(size_t)t * k + lane] = my_w;
+    }
+    if (nonfinite && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();   // this CTA's picks are visible before its ticket
+    last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();   // every other CTA's picks, published before their tickets
+  for (int i = threadIdx.x; i < 32 * E; i += kSmallRouteThreads) cnt[i] = 0;
+  __syncthreads();
+  // counts per warp of assignments, rank inside the warp
+  const int P = T * k;
+  const int a = threadIdx.x;
+  int e = a < P ? __ldcg(topk_idx + a) : -1;
+  if (e >= E) e = -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank_w == 0) cnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  // per expert: the warps' bases (prefix over warps) and the total
+  int total_e = 0;
+  if (threadIdx.x < E) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = cnt[w * E + threadIdx.x];
+      cnt[w * E + threadIdx.x] = run;
+      run += v;
+    }
+    total_e = run;
+  }
+  int total;
+  const int off = block_exclusive_scan(threadIdx.x < E ? total_e : 0, &total, warp_sums);
+  if (threadIdx.x < E) {
+    counts[threadIdx.x] = total_e;
+    offsets[threadIdx.x] = off;
+    off_s[threadIdx.x] = off;
+  }
+  if (threadIdx.x == 0) offsets[E] = total;
+  write_block_plan(threadIdx.x, E, total_e, beta, block_off, num_blocks, block_expert,
+                   warp_sums);
+  __syncthreads();
+  // the stable scatter, with the -1 markers of the chunked kernels
+  if (e >= 0) {
+    const int pos = off_s[e] + cnt[warp * E + e] + rank_w;
+    sorted_src[pos] = a;
+    dest_of[a] = pos;
+  } else if (a < P) {
+    dest_of[a] = -1;
+  }
+  if (a < P && a >= total) sorted_src[a] = -1;
+  if (threadIdx.x == 0) *ticket = 0;   // for the next launch
+}
+
 // x_perm[p] = x[sorted_src[p] / k]: one warp per segment of 4 x 32 16-byte
 // vectors of a row (segments grid-strided), all four loads of a lane in
 // flight before its stores.  Positions holding -1 (no assignment) are skipped.
@@ -247,6 +341,27 @@ cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int3
                         int beta, cudaStream_t s, bool pdl) {
   return launch_k(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, pdl, chunk_hist, C, E, counts,
                   offsets, block_off, num_blocks, block_expert, beta);
+}
+
+cudaError_t launch_route_permute_small(const float* logits, int T, int E, int k, int beta,
+                                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                      int32_t* offsets, int32_t* block_off, int32_t* num_blocks,
+                                      int32_t* block_expert, int32_t* sorted_src,
+                                      int32_t* dest_of, int* ticket, int* status,
+                                      cudaStream_t s) {
+  if (!route_permute_small_ok(T, E, k)) return cudaErrorInvalidValue;
+  if (T == 0) return cudaSuccess;
+  const int grid = (T + kSmallRouteThreads / 32 - 1) / (kSmallRouteThreads / 32);
+#define MOE_SMALL_ROUTE(N)                                                                   \
+  route_permute_small_kernel<N><<<grid, kSmallRouteThreads, 0, s>>>(                           \
+      logits, T, E, k, beta, topk_idx, topk_w, counts, offsets, block_off, num_blocks,         \
+      block_expert, sorted_src, dest_of, ticket, status)
+  if (E <= 32) MOE_SMALL_ROUTE(1);
+  else if (E <= 64) MOE_SMALL_ROUTE(2);
+  else if (E <= 128) MOE_SMALL_ROUTE(4);
+  else MOE_SMALL_ROUTE(8);
+#undef MOE_SMALL_ROUTE
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int P, int32_t* block_off,
