@@ -297,6 +297,42 @@ def time_forward(moe, wl, d, ws, K, warmup, world, dev, sample_clocks, local=0):
     return region_ms / K, (clocks.summary() if clocks else None), flush
 
 
+def time_graph(moe, wl, d, K, warmup, dev, flush):
+    """K launches of the layer captured once as a CUDA graph (moe.ForwardGraph,
+    its own workspace), on a side stream, under the same L2 rule as
+    time_forward (flushed before every step and each step between its own
+    events when the weights fit in L2).  Returns ms per step."""
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        g = moe.ForwardGraph(d["x"], d["logits"], d["W1"], d["W3"], d["W2"], wl.k, out=out)
+        for _ in range(warmup):
+            g.launch()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        s.synchronize()
+        t0.record()
+        for i in range(K):
+            if flush:
+                flush_buf.zero_()
+                evs[i][0].record()
+            g.launch()
+            if flush:
+                evs[i][1].record()
+        t1.record()
+        s.synchronize()
+        st = moe.moe_get_device_status(g.ws)
+        g.close()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    if st != 0:
+        raise RuntimeError(f"device status after graph launches: {moe.moe_status_string(st)}")
+    region = sum(e[0].elapsed_time(e[1]) for e in evs) if flush else t0.elapsed_time(t1)
+    return region / K
+
+
 def time_stages(moe, wl, d, ws, K, dev, flush):
     """K moe_forward_events steps: each kernel's mean duration, from one CUDA
     event between consecutive kernels on the launch stream."""
@@ -386,6 +422,8 @@ def bench_ours(args, rank, world, local):
     value = throughput(world, wl.T, K, ms_per_step * K)
     # the per-kernel breakdown: a second region with stage events
     mean_ms, events_ms_per_step = time_stages(moe, wl, d, ws, K, dev, flush)
+    # the same layer captured once as a CUDA graph and replayed (no host launches)
+    graph_ms = time_graph(moe, wl, d, K, args.warmup, dev, flush) if world == 1 else None
 
     # end to end: host activations in, host result out, through the C ABI
     e2e = None
@@ -444,11 +482,16 @@ def bench_ours(args, rank, world, local):
         "kernels_timing": ("per-stage CUDA events on the launch stream, in a second timed "
                            f"region of {K} moe_forward_events steps "
                            f"({events_ms_per_step:.4f} ms per step with the events)"),
-        "gpu_launches": moe.FORWARD_STAGES * K,
+        "gpu_launches": acc.forward_launches(wl.T, wl.k, wl.E) * K,
         "clocks": clocks,
     }
     if e2e:
         result["e2e"] = e2e
+    if graph_ms is not None:
+        result["graph"] = {"ms_per_step": round(graph_ms, 5),
+                           "value": round(wl.T / graph_ms * 1e3, 1), "unit": UNIT,
+                           "how": "moe.ForwardGraph: the layer captured once as a CUDA graph, "
+                                  f"{K} launches, same L2 rule as the value"}
     if world == 1 and not args.no_configs:
         result["configs"] = bench_configs(moe, args, pool, ws, dev, wl.name, ms_per_step)
     if world == 1 and not args.no_protocol:
@@ -473,6 +516,7 @@ def bench_configs(moe, args, pool, ws, dev, main_name, main_ms):
         K = max(10, args.steps)
         ms, clocks, flush = time_forward(moe, wl, d, ws, K, max(3, args.warmup), 1, dev, True)
         mean_ms, _ = time_stages(moe, wl, d, ws, K, dev, flush)
+        graph_ms = time_graph(moe, wl, d, K, max(3, args.warmup), dev, flush)
         times[name] = ms
         lay = layer_roofline(wl, ms, touched, peaks)
         roof = kernel_roofline(wl, mean_ms, touched, peaks, peak_src)
@@ -484,6 +528,8 @@ def bench_configs(moe, args, pool, ws, dev, main_name, main_ms):
                      "kernel_bound": roof["bound"], "kernel_ms": roof["kernel_ms"],
                      "touched_experts": touched, "max_expert_count": max_count,
                      "l2": "flushed between steps" if flush else "inputs larger than L2",
+                     "graph_ms_per_step": round(graph_ms, 5),
+                     "graph_layer_frac": layer_roofline(wl, graph_ms, touched, peaks)["frac"],
                      "steps": K, "clocks": clocks}
         del d
     if "fine_grained" in times:

@@ -6,6 +6,7 @@ kernels.  Importing the package does not load the library; the first call
 does, and raises if libmoe.so has not been built (there is no fallback).
 """
 from .binding import (  # noqa: F401
+    ForwardGraph,
     MoeError,
     load_library,
     moe_combine,

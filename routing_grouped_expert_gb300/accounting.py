@@ -78,6 +78,14 @@ def ffn_gathers_rows(T: int, k: int, E: int) -> bool:
     return T * k <= 40 * E
 
 
+def forward_launches(T: int, k: int, E: int) -> int:
+    """Kernels one moe_forward launches: routing (one kernel when T*k <= 1024
+    and E <= 256, else route, scan and scatter), the gather unless FC1 gathers
+    its rows itself, FC1, FC2 and the combine."""
+    routing = 1 if (T * k <= 1024 and E <= 256) else 3
+    return routing + (0 if ffn_gathers_rows(T, k, E) else 1) + 3
+
+
 def fc1_bytes(H: int, F: int, touched: int, T: int, k: int, E: int) -> int:
     """W1 and W3 of touched experts + the token rows read + h written.  The
     rows are x itself (each of its T rows read once from HBM) when FC1

@@ -47,6 +47,10 @@ SIGNATURES = {
     "moe_forward_gated": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                                _VP, _VP, _SZ, _VP]),
     "moe_forward_f32": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ, _VP]),
+    "moe_forward_graph_create": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _SZ,
+                                      _VP, ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_graph_launch": (_I, [_VP, _VP]),
+    "moe_graph_destroy": (_I, [_VP]),
     "moe_cast_bf16": (_I, [_VP, _VP, _SZ, _VP]),
     "moe_forward_routing": (_I, [_VP, _SZ, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP]),
@@ -249,6 +253,53 @@ def moe_forward(x, router_logits, W1, W3, W2, k: int, out=None, ws: Workspace | 
 
 
 FORWARD_STAGES = 7
+
+
+class ForwardGraph:
+    """moe_forward captured once into a CUDA graph on the current stream (which
+    must not be the legacy default stream): launch() runs the whole layer on
+    the current stream, reading x and router_logits and writing out as they
+    are then.  The tensors given here, and the workspace memory captured (a
+    private workspace unless one is given), are kept alive by this object;
+    refill x and router_logits in place between launches."""
+
+    def __init__(self, x, router_logits, W1, W3, W2, k: int, out=None,
+                 ws: Workspace | None = None):
+        T, H = x.shape
+        E, _, F = W1.shape
+        _need(x, torch.bfloat16, (T, H), "x")
+        _need(router_logits, torch.float32, (T, E), "router_logits")
+        _need(W1, torch.bfloat16, (E, H, F), "W1")
+        _need(W3, torch.bfloat16, (E, H, F), "W3")
+        _need(W2, torch.bfloat16, (E, F, H), "W2")
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device) if out is None else out
+        _need(out, torch.bfloat16, (T, H), "out")
+        if ws is None:
+            ws = Workspace(x.device)
+        ws.ensure(moe_workspace_size(T, H, F, E, k))
+        # the captured pointers: kept alive even if `ws` later grows elsewhere
+        self.tensors = (x, router_logits, W1, W3, W2, out, ws.buf)
+        self.ws, self.out = ws, out
+        self._h = ctypes.c_void_p()
+        _check(load_library().moe_forward_graph_create(
+            _p(x), _p(router_logits), _p(W1), _p(W3), _p(W2), T, H, F, E, k, _p(out), ws.ptr,
+            ws.nbytes, _stream(), ctypes.byref(self._h)), "moe_forward_graph_create")
+
+    def launch(self):
+        _check(load_library().moe_graph_launch(self._h, _stream()), "moe_graph_launch")
+        return self.out
+
+    def close(self):
+        """Free the graph (after its last launch has completed)."""
+        if self._h:
+            _check(load_library().moe_graph_destroy(self._h), "moe_graph_destroy")
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_forward_f32(x, router_logits, W1, W3, W2, k: int, out=None,

@@ -6,6 +6,8 @@
 
 #include <atomic>
 
+#include <new>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -302,6 +304,71 @@ moe_status moe_forward(const void* x, const float* router_logits, const void* W1
   if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
   return forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L,
                         static_cast<cudaStream_t>(stream));
+}
+
+// A captured moe_forward: the graph and its executable instance.
+struct moe_graph_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+moe_status moe_forward_graph_create(const void* x, const float* router_logits, const void* W1,
+                                    const void* W3, const void* W2, int T, int H, int F, int E,
+                                    int k, void* out, void* ws, size_t ws_bytes, void* stream,
+                                    moe_graph* graph) {
+  if (graph == nullptr) return MOE_ERR_INVALID_ARG;
+  *graph = nullptr;
+  if (!ok_sizes(T, H, F, E, k) || T == 0) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(x) || !ok_ptr(router_logits) || !ok_ptr(W1) || !ok_ptr(W3) || !ok_ptr(W2) ||
+      !ok_ptr(out))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, F, E, k);
+  if (check_ws(ws, ws_bytes, L.total) != MOE_OK) return MOE_ERR_WORKSPACE;
+  if (!device_is_sm103()) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;   // the legacy stream cannot be captured
+  cudaStreamCaptureStatus cs;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return MOE_ERR_INVALID_ARG;
+  // Only this thread's work on `s` is recorded; nothing runs until a launch.
+  MOE_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  const moe_status st = forward_device(x, router_logits, W1, W3, W2, T, H, F, E, k, out, ws, L, s);
+  cudaGraph_t g = nullptr;
+  const cudaError_t end = cudaStreamEndCapture(s, &g);
+  if (st != MOE_OK || end != cudaSuccess) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return st != MOE_OK ? st : MOE_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  moe_graph h = new (std::nothrow) moe_graph_s;
+  if (h == nullptr) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(g);
+    return MOE_ERR_CUDA;
+  }
+  h->graph = g;
+  h->exec = exec;
+  *graph = h;
+  return MOE_OK;
+}
+
+moe_status moe_graph_launch(moe_graph graph, void* stream) {
+  if (graph == nullptr) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_graph_destroy(moe_graph graph) {
+  if (graph == nullptr) return MOE_OK;
+  const cudaError_t a = cudaGraphExecDestroy(graph->exec);
+  const cudaError_t b = cudaGraphDestroy(graph->graph);
+  delete graph;
+  return cuda_status(a != cudaSuccess ? a : b);
 }
 
 moe_status moe_forward_f32(const void* x, const float* router_logits, const void* W1,
