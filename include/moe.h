@@ -209,8 +209,8 @@ moe_status moe_forward(const void* x, const float* router_logits,
  * 0.707 ms; large layers run slower from a graph, e.g. a 4096-token, 16-expert
  * prefill chunk 3.82 -> 4.08 ms).  moe_forward_graph_create records one
  * moe_forward with exactly these arguments on `stream` (a non-default
- * stream, not capturing; only the
- * calling thread's work is recorded) and instantiates it; nothing runs.
+ * stream, not capturing; only the calling thread's work is recorded) and
+ * instantiates it; nothing runs.
  * moe_graph_launch enqueues the whole layer on `stream`: it reads x and
  * router_logits and writes out, ws as they are at that time (same pointers,
  * same sizes, same weights), so a caller refills x and router_logits in place
