@@ -65,15 +65,60 @@ __device__ __forceinline__ void write_block_plan(int e, int E, int cnt, int beta
   }
 }
 
+// The chunk table [C][E] is staged in shared memory when it fits (every
+// thread's loads in flight at once, instead of C / 8 dependent rounds of loads
+// per expert); larger tables are read in place.
+constexpr int kScanSmemMax = 160 * 1024;
+__host__ __device__ inline bool scan_in_smem(int C, int E) {
+  return (size_t)C * E * 4 <= kScanSmemMax;
+}
+
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int32_t* __restrict__ chunk_hist, int C, int E, int32_t* __restrict__ counts,
             int32_t* __restrict__ offsets, int32_t* __restrict__ block_off,
             int32_t* __restrict__ num_blocks, int32_t* __restrict__ block_expert, int beta) {
   __shared__ int warp_sums[33];
+  extern __shared__ int hist_s[];   // [C][E] when staged
   pdl_wait();
   pdl_trigger();
   const int e = threadIdx.x;
   constexpr int kBatch = 8;   // loads in flight per thread
+  if (scan_in_smem(C, E)) {
+    const int n = C * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += kBatch * kScanThreads) {
+      int v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * kScanThreads;
+        v[b] = i < n ? chunk_hist[i] : 0;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * kScanThreads;
+        if (i < n) hist_s[i] = v[b];
+      }
+    }
+    __syncthreads();
+    int cnt = 0;
+    if (e < E)
+      for (int c = 0; c < C; ++c) cnt += hist_s[c * E + e];
+    int total;
+    const int off = block_exclusive_scan(e < E ? cnt : 0, &total, warp_sums);
+    if (e < E) {
+      counts[e] = cnt;
+      offsets[e] = off;
+      // chunk c's rows of expert e start at off + (its rows in chunks < c)
+      int run = off;
+      for (int c = 0; c < C; ++c) {
+        const int v = hist_s[c * E + e];
+        chunk_hist[(size_t)c * E + e] = run;
+        run += v;
+      }
+    }
+    if (e == 0) offsets[E] = total;
+    write_block_plan(e, E, cnt, beta, block_off, num_blocks, block_expert, warp_sums);
+    return;
+  }
   int cnt = 0;
   if (e < E) {
     // the expert's count over all chunks (loads only, batched)
@@ -339,7 +384,13 @@ gather_tokens_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restr
 cudaError_t launch_scan(int32_t* chunk_hist, int C, int E, int32_t* counts, int32_t* offsets,
                         int32_t* block_off, int32_t* num_blocks, int32_t* block_expert,
                         int beta, cudaStream_t s, bool pdl) {
-  return launch_k(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, pdl, chunk_hist, C, E, counts,
+  const size_t smem = scan_in_smem(C, E) ? (size_t)C * E * 4 : 0;
+  if (smem > 48 * 1024) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemMax);
+    if (attr != cudaSuccess) return attr;
+  }
+  return launch_k(scan_kernel, dim3(1), dim3(kScanThreads), smem, s, pdl, chunk_hist, C, E, counts,
                   offsets, block_off, num_blocks, block_expert, beta);
 }
 
